@@ -1,0 +1,463 @@
+"""Benchmark of the GB300 routed-expert MoE layer (one JSON line on stdout).
+
+Metric: MoE-layer tokens per second -- tokens pushed through one MoE layer per
+second, summed over the layers of a step and over all ranks.
+
+Workloads (``--workload``, default ``decode``):
+  decode            T = 1 token through 10 stacked, distinct MoE layers per step
+                    (d = 2048, 256 experts of inner size 512, top-8 + shared),
+                    each layer with its own token; 10 x ~59 MB of weights per
+                    step, far larger than L2, so no flush is needed.
+  prefill_balanced  T = 4096 tokens through one layer (1.6 GB of weights > L2).
+  prefill_skewed    same with the Zipf-like router bias.
+  sweep_T<n>        one layer at T = n.
+
+Timing: W untimed warm-up steps, then exactly K steps replayed from CUDA graphs
+and bracketed by a barrier and a device synchronisation on both sides, CUDA
+events on the launching stream, max over ranks.  The dominant kernel of the
+path is bracketed by its own CUDA events inside the replayed graph (through the
+library's profiling hook), which gives its average launch duration for the
+roofline.  ``e2e`` repeats the measurement with each step's x copied in from
+pinned host memory and y copied back out, inside the timed region.
+
+Multi-GPU (torchrun): every rank runs the same workload on its own GPU (data
+parallel replicas, no collective on the data path); ``value`` counts the
+tokens of all ranks over the slowest rank's time.
+
+``--impl reference`` times the fp64 CPU oracle (the only reference there is) on
+a bounded sample of the same workload on the host cores.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import moe_workloads as mw  # noqa: E402
+
+METRIC = "MoE-layer tokens/s (decode T=1, prefill T=4096) on 1 GB300; % HBM / bf16 roofline"
+UNIT = "tokens/s"
+GRAPH_STEPS = 50  # steps per captured graph; longer runs replay it
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            j = json.load(f)
+        return dict(hbm_gbs=j["hbm_gbs"], bf16_tflops=j["bf16_tflops"],
+                    bf16_tflops_sustained=j.get("bf16_tflops_sustained", j["bf16_tflops"]), source="measured")
+    return dict(hbm_gbs=6800.0, bf16_tflops=1900.0, bf16_tflops_sustained=1700.0, source="fallback")
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    """nvidia-smi samples (200 ms) of SM clock and throttle reasons."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,utilization.gpu,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.t = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return dict(sm_mhz=None, sm_max_mhz=None, reasons=["nvidia-smi unavailable"], samples=0)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.t.join(timeout=2)
+        rows = []
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 10:
+                continue
+            try:
+                rows.append(dict(sm=float(parts[1]), smax=float(parts[2]), util=float(parts[4]),
+                                 hw=parts[6], hwt=parts[7], swt=parts[8], pcap=parts[9]))
+            except ValueError:
+                continue
+        if not rows:
+            return dict(sm_mhz=None, sm_max_mhz=None, reasons=["no samples"], samples=0)
+        busy = [r for r in rows if r["util"] > 0] or rows
+        reasons = sorted({name for r in busy for name, key in
+                          (("hw_slowdown", "hw"), ("hw_thermal_slowdown", "hwt"), ("sw_thermal_slowdown", "swt"),
+                           ("sw_power_cap", "pcap")) if r[key].lower() == "active"})
+        return dict(sm_mhz=statistics.median(r["sm"] for r in busy), sm_max_mhz=max(r["smax"] for r in rows),
+                    reasons=reasons, samples=len(busy))
+
+
+# ------------------------------------------------------------------ inputs
+def device_weights(w: mw.Workload, layer: int, dev):
+    """Seeded device-side weights of one layer (torch CUDA generator)."""
+    import torch
+
+    g = torch.Generator(device=dev)
+    g.manual_seed(w.seed * 1000 + layer)
+
+    def normal(*shape):
+        out = torch.empty(*shape, dtype=torch.bfloat16, device=dev)
+        flat = out.view(-1)
+        step = 1 << 26
+        for i in range(0, flat.numel(), step):
+            n = min(step, flat.numel() - i)
+            flat[i:i + n] = (torch.randn(n, generator=g, device=dev) * 0.02).to(torch.bfloat16)
+        return out
+
+    router_w = torch.randn(w.E, w.d, generator=g, device=dev) * 0.02
+    router_b = None
+    if w.skewed:
+        router_b = torch.tensor(mw.draw_router(w, layer)[1], device=dev)
+    return dict(router_w=router_w.contiguous(), router_b=router_b, gate_up=normal(w.E, 2 * w.I, w.d),
+                down=normal(w.E, w.d, w.I), shared=normal(3 * w.I_s * w.d) if w.I_s else None)
+
+
+def host_x(w: mw.Workload, layer: int):
+    import torch
+
+    x = mw.draw_x(w, layer)
+    if w.x_dtype == "f32":
+        return torch.from_numpy(x)
+    return torch.from_numpy(x.view(np.int16)).view(torch.bfloat16)
+
+
+# ------------------------------------------------------------------ algorithmic bytes / flops
+def layer_costs(w: mw.Workload, idx: np.ndarray):
+    """Bytes and flops a layer must move/compute, from its actual routing."""
+    distinct = len(np.unique(idx)) + (1 if w.I_s else 0)
+    expert_bytes = 3 * w.d * w.I * 2
+    xb = 2 if w.x_dtype == "bf16" else 4
+    rows = w.T * (w.k + (1 if w.I_s else 0))
+    return dict(
+        distinct=distinct,
+        gate_up_bytes=distinct * 2 * w.I * w.d * 2 + w.T * w.d * xb,
+        layer_bytes=distinct * expert_bytes + w.E * w.d * 4 + 2 * w.T * w.d * xb,
+        gate_up_flops=2.0 * rows * w.d * 2 * w.I,
+        layer_flops=2.0 * rows * 3 * w.d * w.I,
+    )
+
+
+def dominant_kernel(path: int):
+    import expert_routed_ffn_moe_gb300 as moe
+
+    return moe.MOE_K_GEMV_GATE_UP if path == moe.MOE_PATH_GEMV else moe.MOE_K_GEMM_GATE_UP
+
+
+# ------------------------------------------------------------------ oracle leg
+def oracle_sample(w: mw.Workload, budget_s: float, host_inputs, seed=0):
+    """Time the fp64 oracle on a bounded sample of tokens; returns (tokens/s, tokens, seconds, threads)."""
+    import oracle
+
+    threads = int(os.environ.get("OPENBLAS_NUM_THREADS", os.cpu_count() or 1))
+    rng = np.random.default_rng(seed)
+    done, t0 = 0, time.perf_counter()
+    while True:
+        for layer, inp in enumerate(host_inputs):
+            n = min(w.T, 8)
+            toks = np.sort(rng.choice(w.T, n, replace=False))
+            oracle.moe_layer(inp["x"], inp["router_w"], inp["router_b"], inp["gate_up"], inp["down"], inp["shared"],
+                             w.k, x_bf16=w.x_dtype == "bf16", tokens=toks, expert_ids=inp["expert_ids"])
+            done += n
+        el = time.perf_counter() - t0
+        if el >= budget_s:
+            return done / el, done, el, threads
+
+
+def host_layer_for_oracle(w, layer, dev_w, x_host, idx_dev):
+    """Host copies of what the oracle needs for one layer: x, router, the used experts, shared."""
+    def bits(t):
+        return t.contiguous().view(__import__("torch").int16).cpu().numpy().view(np.uint16)
+
+    used = np.unique(idx_dev)
+    return dict(x=(x_host.numpy() if w.x_dtype == "f32" else bits(x_host)),
+                router_w=dev_w["router_w"].cpu().numpy(),
+                router_b=None if dev_w["router_b"] is None else dev_w["router_b"].cpu().numpy(),
+                gate_up=bits(dev_w["gate_up"][used]), down=bits(dev_w["down"][used]),
+                shared=None if dev_w["shared"] is None else bits(dev_w["shared"]), expert_ids=used)
+
+
+# ------------------------------------------------------------------ main arm
+def run_ours(args, rank, world, dev):
+    import torch
+
+    import expert_routed_ffn_moe_gb300 as moe
+
+    moe.build()
+    w = mw.WORKLOADS[args.workload]
+    layers = w.layers
+    peaks = load_peaks()
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.Stream(device=dev)
+
+    weights = [device_weights(w, L, dev) for L in range(layers)]
+    xh = [host_x(w, L).pin_memory() for L in range(layers)]
+    xd = [t.to(dev) for t in xh]
+    yd = [torch.empty_like(t) for t in xd]
+    yh = [torch.empty_like(t).pin_memory() for t in xh]
+    ctx = moe.MoeLayer(w.d, w.E, w.I, w.k, w.T, x_dtype=moe.MOE_F32 if w.x_dtype == "f32" else moe.MOE_BF16,
+                       has_router_bias=w.skewed, has_shared=w.I_s > 0)
+    path = moe.MOE_PATH_AUTO if args.path == "auto" else (moe.MOE_PATH_GEMV if args.path == "gemv"
+                                                          else moe.MOE_PATH_GEMM)
+    moe.moe_set_path(ctx.ctx, path)
+    eff_path = path if path != moe.MOE_PATH_AUTO else (moe.MOE_PATH_GEMV if w.T <= 8 else moe.MOE_PATH_GEMM)
+    dom = dominant_kernel(eff_path)
+
+    def step(ev_pairs=None, e2e=False):
+        for L in range(layers):
+            if e2e:
+                xd[L].copy_(xh[L], non_blocking=True)
+            if ev_pairs is not None:
+                moe.moe_time_kernel(ctx.ctx, dom, *ev_pairs[L])
+            p = weights[L]
+            moe.moe_forward(ctx.ctx, xd[L], p["router_w"], p["router_b"], p["gate_up"], p["down"], p["shared"], w.k,
+                            yd[L], stream)
+            if e2e:
+                yh[L].copy_(yd[L], non_blocking=True)
+
+    # routing of every layer (for the algorithmic byte counts) and warm-up
+    costs = []
+    with torch.cuda.stream(stream):
+        for L in range(layers):
+            p = weights[L]
+            r = ctx.route(xd[L], p["router_w"], p["router_b"], stream=stream)
+            costs.append(layer_costs(w, r["idx"].cpu().numpy()))
+        for _ in range(max(args.warmup, 0)):
+            step()
+    stream.synchronize()
+    if ctx.status() != moe.MOE_OK:
+        raise RuntimeError("device status after warm-up: " + moe.moe_strerror(ctx.status()))
+
+    def make_events(n):
+        evs = []
+        for _ in range(n):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            b.record(stream)
+            evs.append((a, b))
+        return evs
+
+    def capture(n_steps, e2e, with_events):
+        g = torch.cuda.CUDAGraph()
+        evs = make_events(n_steps * layers) if with_events else None
+        stream.synchronize()
+        before = moe.moe_launch_count(ctx.ctx)
+        with torch.cuda.graph(g, stream=stream):
+            for s in range(n_steps):
+                step(evs[s * layers:(s + 1) * layers] if evs else None, e2e)
+        launches = moe.moe_launch_count(ctx.ctx) - before
+        return g, evs, launches
+
+    def timed(n_steps, e2e):
+        gsteps = min(n_steps, GRAPH_STEPS)
+        g, evs, launches_per_graph = capture(gsteps, e2e, with_events=not e2e)
+        reps, rem = divmod(n_steps, gsteps)
+        g_rem = capture(rem, e2e, with_events=False)[0] if rem else None
+        with torch.cuda.stream(stream):
+            g.replay()  # untimed: uploads the graph
+            if g_rem:
+                g_rem.replay()
+        stream.synchronize()
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize(dev)
+        start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            start.record(stream)
+            for _ in range(reps):
+                g.replay()
+            if g_rem:
+                g_rem.replay()
+            stop.record(stream)
+        stop.synchronize()
+        torch.cuda.synchronize(dev)
+        if world > 1:
+            torch.distributed.barrier()
+        ms = start.elapsed_time(stop)
+        kern = [a.elapsed_time(b) for a, b in evs] if evs else []
+        total_launches = launches_per_graph * reps + (launches_per_graph // gsteps) * rem
+        return ms, kern, total_launches
+
+    clocks = ClockSampler(torch.cuda.current_device())
+    clocks.start()
+    time.sleep(0.3)
+    ms, kern_ms, launches = timed(args.steps, e2e=False)
+    clk = clocks.stop()
+    ms_e2e, _, _ = timed(args.steps, e2e=True)
+    if ctx.status() != moe.MOE_OK:
+        raise RuntimeError("device status after timing: " + moe.moe_strerror(ctx.status()))
+
+    if world > 1:
+        t = torch.tensor([ms, ms_e2e], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms, ms_e2e = t.tolist()
+    ms_step = ms / args.steps
+    tokens_step = w.T * layers
+    value = tokens_step * world / (ms_step / 1e3)
+    e2e_value = tokens_step * world / (ms_e2e / args.steps / 1e3)
+
+    # roofline of the dominant kernel: algorithmic bytes (or flops) per launch / mean launch time
+    kern_avg_ms = statistics.mean(kern_ms) if kern_ms else None
+    if eff_path == moe.MOE_PATH_GEMV:
+        per_launch = statistics.mean(c["gate_up_bytes"] for c in costs)
+        achieved = per_launch / (kern_avg_ms / 1e3) / 1e9
+        roof = dict(bound="hbm", achieved=round(achieved, 1), peak=peaks["hbm_gbs"], unit="GB/s",
+                    frac=round(achieved / peaks["hbm_gbs"], 4), traffic=None,
+                    kernel="gemv_gate_up_kernel", algorithmic_bytes_per_launch=int(per_launch),
+                    avg_launch_us=round(kern_avg_ms * 1e3, 2), peak_source=peaks["source"])
+    else:
+        per_launch_b = statistics.mean(c["gate_up_bytes"] for c in costs)
+        per_launch_f = statistics.mean(c["gate_up_flops"] for c in costs)
+        gbs = per_launch_b / (kern_avg_ms / 1e3) / 1e9
+        tfs = per_launch_f / (kern_avg_ms / 1e3) / 1e12
+        hbm_frac, tc_frac = gbs / peaks["hbm_gbs"], tfs / peaks["bf16_tflops"]
+        if hbm_frac >= tc_frac:
+            roof = dict(bound="hbm", achieved=round(gbs, 1), peak=peaks["hbm_gbs"], unit="GB/s",
+                        frac=round(hbm_frac, 4), traffic=None)
+        else:
+            roof = dict(bound="tensor", achieved=round(tfs, 1), peak=peaks["bf16_tflops"], unit="TFLOP/s",
+                        frac=round(tc_frac, 4), traffic=None)
+        roof.update(kernel="grouped_gemm_kernel<gate_up>", algorithmic_bytes_per_launch=int(per_launch_b),
+                    algorithmic_flops_per_launch=int(per_launch_f), avg_launch_us=round(kern_avg_ms * 1e3, 2),
+                    tensor_frac=round(tc_frac, 4), hbm_frac=round(hbm_frac, 4), peak_source=peaks["source"])
+    layer_bytes = statistics.mean(c["layer_bytes"] for c in costs)
+    layer_flops = statistics.mean(c["layer_flops"] for c in costs)
+    ms_layer = ms_step / layers
+    whole = dict(ms_per_layer=round(ms_layer, 5),
+                 hbm_frac_of_layer=round(layer_bytes / (ms_layer / 1e3) / 1e9 / peaks["hbm_gbs"], 4),
+                 tensor_frac_of_layer=round(layer_flops / (ms_layer / 1e3) / 1e12 / peaks["bf16_tflops"], 4),
+                 algorithmic_bytes_per_layer=int(layer_bytes), algorithmic_flops_per_layer=int(layer_flops),
+                 distinct_experts_per_layer=round(statistics.mean(c["distinct"] for c in costs), 1))
+
+    out = None
+    if rank == 0:
+        cpu = None
+        if not args.no_cpu_baseline and world == 1:
+            hosts = []
+            for L in range(layers):
+                p = weights[L]
+                r = ctx.route(xd[L], p["router_w"], p["router_b"], stream=stream)
+                hosts.append(host_layer_for_oracle(w, L, p, xh[L], r["idx"].cpu().numpy()))
+            v, n, el, thr = oracle_sample(w, args.cpu_seconds, hosts)
+            cpu = dict(value=round(v, 3), unit=UNIT, cores=thr, kind="oracle",
+                       sample=f"{n} token-layers (<=8 random tokens per layer, all {layers} layers, repeated) "
+                              f"in {el:.1f} s; fp64 numpy, BLAS threads = {thr}")
+        out = dict(metric=METRIC, value=round(value, 1), unit=UNIT, n_gpus=world, steps=args.steps,
+                   warmup=args.warmup, ms_per_step=round(ms_step, 5), higher_is_better=True, scaling="weak",
+                   vs_baseline=None, dtype="bf16", data="synthetic",
+                   config=dict(workload=w.name, tokens_per_layer=w.T, layers_per_step=layers, d=w.d, experts=w.E,
+                               inter=w.I, shared_inter=w.I_s, top_k=w.k,
+                               path="gemv" if eff_path == moe.MOE_PATH_GEMV else "grouped_gemm",
+                               l2="inputs larger than L2 (distinct weights per layer, >126 MB per step)",
+                               parallelism=f"replicas x{world}"),
+                   e2e=dict(value=round(e2e_value, 1), unit=UNIT,
+                            h2d_bytes_per_step=int(sum(t.numel() * t.element_size() for t in xh)),
+                            d2h_bytes_per_step=int(sum(t.numel() * t.element_size() for t in yh))),
+                   gpu_launches=int(launches), roofline=roof, layer=whole, clocks=clk, cpu_baseline=cpu)
+    ctx.close()
+    return out
+
+
+def run_reference(args):
+    """The fp64 oracle on the host cores, on a bounded sample of the same workload."""
+    w = mw.WORKLOADS[args.workload]
+    import oracle  # noqa: F401  (test infrastructure; this leg times it as the CPU baseline)
+
+    hosts = []
+    for L in range(w.layers):
+        wr, b = mw.draw_router(w, L)
+        x = mw.draw_x(w, L)
+        import oracle as orc
+        logits = orc.router_logits(orc.as_f64(x, w.x_dtype == "bf16"), wr.astype(np.float64), b)
+        idx, _, _ = orc.route(logits, w.k)
+        used = np.unique(idx)
+        gu, dn = mw.draw_experts(w, L, used)
+        hosts.append(dict(x=x, router_w=wr, router_b=b, gate_up=gu, down=dn, shared=mw.draw_shared(w, L),
+                          expert_ids=used))
+    for _ in range(max(args.warmup, 0)):
+        oracle_sample(w, 0.0, hosts)
+    per = []
+    for _ in range(args.steps):
+        v, n, el, thr = oracle_sample(w, args.ref_step_seconds, hosts)
+        per.append((n, el))
+    n = sum(a for a, _ in per)
+    el = sum(b for _, b in per)
+    value = n / el
+    return dict(metric=METRIC, value=round(value, 3), unit=UNIT, n_gpus=1, steps=args.steps, warmup=args.warmup,
+                ms_per_step=round(el / args.steps * 1e3, 3), higher_is_better=True, scaling="weak",
+                vs_baseline=None, dtype="f64", data="synthetic", impl="reference",
+                config=dict(workload=w.name, tokens_per_layer=w.T, layers_per_step=w.layers, d=w.d, experts=w.E,
+                            inter=w.I, top_k=w.k),
+                cpu_baseline=dict(value=round(value, 3), unit=UNIT, cores=thr, kind="oracle",
+                                  sample=f"{n} token-layers in {el:.1f} s"),
+                e2e=dict(value=round(value, 3), unit=UNIT, h2d_bytes_per_step=0, d2h_bytes_per_step=0))
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="decode", choices=sorted(mw.WORKLOADS))
+    ap.add_argument("--path", default="auto", choices=["auto", "gemv", "gemm"])
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--ref-step-seconds", type=float, default=3.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args)), flush=True)
+        return
+
+    import torch
+
+    dev = torch.device("cuda", local)
+    if world > 1:
+        torch.cuda.set_device(dev)
+        torch.distributed.init_process_group("nccl", device_id=dev)
+    out = run_ours(args, rank, world, dev)
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,423 @@
+// C ABI of the MoE layer: argument checking, the context and its scratch
+// memory, TMA tensor maps, and the per-call kernel sequence.  Declarations and
+// the full contract are in include/moe.h.
+#include <stdio.h>
+#include <stdlib.h>
+#include <string.h>
+
+#include "moe_internal.h"
+
+using namespace moe;
+
+// signature of the driver's cuTensorMapEncodeTiled (fetched at run time, so the
+// library needs no link-time dependency on libcuda)
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+struct moe_ctx {
+  moe_config cfg;
+  int device = 0;
+  int num_sms = 0;
+  int path = MOE_PATH_AUTO;
+  int router = MOE_ROUTER_AUTO;
+  long long spin_ns = 0;
+  int gemv_max_t = 0;       // largest T the GEMV kernels accept for this shape (0: none)
+  void* block = nullptr;    // the single device allocation holding all scratch
+  Scratch sc{};
+  EncodeTiledFn encode = nullptr;
+  // profiling hook (moe_time_kernel) and launch counter
+  int timed_kernel = -1;
+  cudaEvent_t ev_start = nullptr, ev_stop = nullptr;
+  long long launches = 0;
+};
+
+namespace {
+
+constexpr long long kDefaultSpinNs = 1000000000LL;  // 1 s
+constexpr int kGemvSmemLimit = 200 * 1024;           // dynamic shared memory of the GEMV kernels
+
+int cuda_fail(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+// GEMV path limits: x of all T tokens and h of all T*(k+1) rows live in shared memory.
+int gemv_limit(const moe_config& c) {
+  if (c.d % 256 != 0 || c.inter % 256 != 0) return 0;
+  const size_t kSmem = kGemvSmemLimit;
+  int best = 0;
+  for (int T = 1; T <= 32 && T <= c.max_tokens; ++T) {
+    const size_t pairs = (size_t)T * c.top_k + (c.has_shared ? T : 0);
+    const size_t xs = (size_t)T * c.d * 4;
+    const size_t hs = pairs * c.inter * 4 + pairs * 8;
+    if (xs <= kSmem && hs <= kSmem) best = T;
+  }
+  return best;
+}
+
+int make_map(moe_ctx* ctx, CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t outer, uint32_t box_inner,
+             uint32_t box_outer) {
+  const cuuint64_t dims[2] = {inner, outer};
+  const cuuint64_t strides[1] = {inner * 2};
+  const cuuint32_t box[2] = {box_inner, box_outer};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r = ctx->encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box,
+                                 estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? MOE_OK : MOE_ERR_CUDA;
+}
+
+int check_route_args(moe_ctx* ctx, const void* x, int T, const float* wr, const float* rb, int top_k) {
+  if (!ctx || T < 0) return MOE_ERR_ARG;
+  if (T == 0) return MOE_OK;
+  const moe_config& c = ctx->cfg;
+  if (!x || !wr) return MOE_ERR_ARG;
+  if (T > c.max_tokens || top_k < 1 || top_k > c.top_k) return MOE_ERR_ARG;
+  if (c.has_router_bias && !rb) return MOE_ERR_ARG;
+  if (!aligned16(x) || !aligned16(wr) || (rb && !aligned16(rb))) return MOE_ERR_ALIGN;
+  return MOE_OK;
+}
+
+Shapes shapes(const moe_ctx* ctx, int T, int top_k) {
+  const moe_config& c = ctx->cfg;
+  Shapes s;
+  s.T = T;
+  s.d = c.d;
+  s.E = c.n_experts;
+  s.I = c.inter;
+  s.k = top_k;
+  s.has_shared = c.has_shared;
+  s.x_bf16 = c.x_dtype == MOE_BF16;
+  return s;
+}
+
+DevCtl devctl(const moe_ctx* ctx) {
+  DevCtl d;
+  d.status = ctx->sc.status;
+  d.spin_limit = ctx->spin_ns;
+  return d;
+}
+
+bool use_tensor_router(const moe_ctx* ctx, const Shapes& s) {
+  if (ctx->router == MOE_ROUTER_SIMT) return false;
+  const bool able = s.x_bf16 && s.E == 256 && s.d % 64 == 0;
+  if (ctx->router == MOE_ROUTER_TENSOR) return able;
+  return able && s.T > 64;
+}
+
+// Every kernel launch goes through `launch`: it counts the launch and, when
+// the profiling hook is armed for this kernel id, records the caller's events
+// around it.
+// Under stream capture an event record must be marked external to become a
+// timeable event-record node of the graph.
+cudaError_t record_event(cudaEvent_t ev, cudaStream_t st) {
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  cudaError_t e = cudaStreamIsCapturing(st, &cs);
+  if (e != cudaSuccess) return e;
+  return cudaEventRecordWithFlags(ev, st, cs == cudaStreamCaptureStatusActive ? cudaEventRecordExternal : 0u);
+}
+
+template <typename F>
+cudaError_t launch(moe_ctx* ctx, int id, cudaStream_t st, F&& f) {
+  const bool timed = ctx->timed_kernel == id;
+  if (timed) {
+    cudaError_t e = record_event(ctx->ev_start, st);
+    if (e != cudaSuccess) return e;
+  }
+  cudaError_t err = f();
+  ++ctx->launches;
+  if (timed && err == cudaSuccess) {
+    err = record_event(ctx->ev_stop, st);
+    ctx->timed_kernel = -1;
+  }
+  return err;
+}
+
+// Steps 1-4 on the device: logits, selection, grouping.
+int run_route(moe_ctx* ctx, const Shapes& s, const void* x, const float* wr, const float* rb, bool tensor,
+              const GemmMaps* maps, cudaStream_t st) {
+  const DevCtl ctl = devctl(ctx);
+  cudaError_t err;
+  int parts = 1;
+  const Scratch& sc = ctx->sc;
+  const int sms = ctx->num_sms;
+  if (tensor) {
+    err = launch(ctx, -2, st, [&] { return launch_router_split_weights(s, wr, sc, st); });
+    if (err != cudaSuccess) return cuda_fail(err);
+    err = launch(ctx, MOE_K_ROUTER, st, [&] { return launch_gemm_router(s, *maps, sc, ctl, sms, st); });
+    if (err != cudaSuccess) return cuda_fail(err);
+    parts = 3;
+  } else {
+    err = launch(ctx, MOE_K_ROUTER, st, [&] { return launch_router_logits_simt(s, x, wr, rb, sc, st); });
+    if (err != cudaSuccess) return cuda_fail(err);
+  }
+  err = launch(ctx, MOE_K_SELECT, st, [&] { return launch_select(s, rb, parts, sc, ctl, st); });
+  if (err != cudaSuccess) return cuda_fail(err);
+  err = launch(ctx, MOE_K_GROUP, st, [&] { return launch_group(s, sc, ctl, st); });
+  ctx->launches += 1;  // the group step is two kernels
+  return cuda_fail(err);
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* moe_strerror(int code) {
+  switch (code) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_ARG: return "invalid argument";
+    case MOE_ERR_ALIGN: return "tensor pointer not 16-byte aligned";
+    case MOE_ERR_UNSUPPORTED: return "shape or device not supported";
+    case MOE_ERR_CUDA: return "CUDA call failed";
+    case MOE_ERR_TIMEOUT: return "a bounded wait inside a kernel ran out";
+    case MOE_ERR_BOUNDS: return "an index read by a kernel was out of range";
+    case MOE_ERR_NOMEM: return "out of device memory";
+    default: return "unknown error";
+  }
+}
+
+int moe_init(const moe_config* cfg, moe_ctx** out) {
+  if (!cfg || !out) return MOE_ERR_ARG;
+  *out = nullptr;
+  const moe_config c = *cfg;
+  if (c.d <= 0 || c.n_experts <= 0 || c.inter <= 0 || c.top_k <= 0 || c.max_tokens <= 0) return MOE_ERR_ARG;
+  if (c.x_dtype != MOE_F32 && c.x_dtype != MOE_BF16) return MOE_ERR_ARG;
+  if (c.top_k > c.n_experts || c.top_k > kMaxTopK) return MOE_ERR_ARG;
+  if (c.n_experts > kMaxExperts || c.d % 256 != 0 || c.inter % 128 != 0) return MOE_ERR_UNSUPPORTED;
+  if (c.has_shared && c.shared_inter != c.inter) return MOE_ERR_UNSUPPORTED;
+  if ((long long)c.max_tokens * (c.top_k + 1) >= (1LL << 31) / 2) return MOE_ERR_UNSUPPORTED;
+
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
+  cudaDeviceProp prop;
+  if (cudaGetDeviceProperties(&prop, dev) != cudaSuccess) return MOE_ERR_CUDA;
+  if (!(prop.major == 10 && prop.minor == 3)) return MOE_ERR_UNSUPPORTED;
+
+  if (prepare_gemm_kernels() != cudaSuccess || prepare_gemv_kernels(kGemvSmemLimit) != cudaSuccess) {
+    cudaGetLastError();
+    return MOE_ERR_CUDA;
+  }
+
+  moe_ctx* ctx = new moe_ctx();
+  ctx->cfg = c;
+  if (!c.has_shared) ctx->cfg.shared_inter = 0;
+  ctx->device = dev;
+  ctx->num_sms = prop.multiProcessorCount;
+  ctx->spin_ns = kDefaultSpinNs;
+  ctx->gemv_max_t = gemv_limit(ctx->cfg);
+
+  void* fn = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+          cudaSuccess ||
+      q != cudaDriverEntryPointSuccess || !fn) {
+    delete ctx;
+    return MOE_ERR_CUDA;
+  }
+  ctx->encode = reinterpret_cast<EncodeTiledFn>(fn);
+
+  // carve the scratch memory out of one allocation
+  const size_t T = c.max_tokens, k = c.top_k, E = c.n_experts, d = c.d, I = c.inter;
+  const size_t nchunk = (T + kChunk - 1) / kChunk;
+  const size_t rows = T * k + T;
+  const size_t tg = ctx->gemv_max_t;
+  const int max_mtiles = (int)(T * k / kBM + E + T / kBM + 2);
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t o = off;
+    off = round_up(off + bytes, 256);
+    return o;
+  };
+  const size_t o_logits = take(3 * T * E * 4);
+  const size_t o_idx = take(T * k * 4);
+  const size_t o_w = take(T * k * 4);
+  const size_t o_cmask = take(nchunk * E * 4);
+  const size_t o_cbase = take(E * nchunk * 4);
+  const size_t o_counts = take((E + 1) * 4);
+  const size_t o_offsets = take((E + 2) * 4);
+  const size_t o_perm = take(rows * 4);
+  const size_t o_slot = take(T * k * 4);
+  const size_t o_mtiles = take((size_t)max_mtiles * sizeof(MTile));
+  const size_t o_meta = take(4 * 4);
+  const size_t o_active = take((E + 1) * 4);
+  const size_t o_tickets = take(4 * 4);
+  const size_t o_xbf = take(c.x_dtype == MOE_F32 ? T * d * 2 : 16);
+  const size_t o_wrs = take(3 * E * d * 2);
+  const size_t o_h = take(rows * I * 2);
+  const size_t o_hg = take(tg ? (tg * k + tg) * I * 4 : 16);
+  const size_t o_out = take(rows * d * 2);
+  const size_t o_status = take(16);
+  if (cudaMalloc(&ctx->block, off) != cudaSuccess) {
+    cudaGetLastError();
+    delete ctx;
+    return MOE_ERR_NOMEM;
+  }
+  if (cudaMemset(ctx->block, 0, off) != cudaSuccess) {
+    cudaFree(ctx->block);
+    delete ctx;
+    return MOE_ERR_CUDA;
+  }
+  char* b = static_cast<char*>(ctx->block);
+  Scratch& sc = ctx->sc;
+  sc.logits = reinterpret_cast<float*>(b + o_logits);
+  sc.idx = reinterpret_cast<int*>(b + o_idx);
+  sc.w = reinterpret_cast<float*>(b + o_w);
+  sc.chunk_mask = reinterpret_cast<unsigned*>(b + o_cmask);
+  sc.chunk_base = reinterpret_cast<int*>(b + o_cbase);
+  sc.counts = reinterpret_cast<int*>(b + o_counts);
+  sc.offsets = reinterpret_cast<int*>(b + o_offsets);
+  sc.perm = reinterpret_cast<int*>(b + o_perm);
+  sc.slot = reinterpret_cast<int*>(b + o_slot);
+  sc.mtiles = reinterpret_cast<MTile*>(b + o_mtiles);
+  sc.meta = reinterpret_cast<int*>(b + o_meta);
+  sc.active = reinterpret_cast<int*>(b + o_active);
+  sc.tickets = reinterpret_cast<unsigned*>(b + o_tickets);
+  sc.x_bf16 = reinterpret_cast<uint16_t*>(b + o_xbf);
+  sc.wr_split = reinterpret_cast<uint16_t*>(b + o_wrs);
+  sc.h = reinterpret_cast<uint16_t*>(b + o_h);
+  sc.h_gemv = reinterpret_cast<float*>(b + o_hg);
+  sc.out = reinterpret_cast<uint16_t*>(b + o_out);
+  sc.status = reinterpret_cast<unsigned*>(b + o_status);
+  sc.max_mtiles = max_mtiles;
+  *out = ctx;
+  return MOE_OK;
+}
+
+int moe_set_path(moe_ctx* ctx, int path) {
+  if (!ctx || path < MOE_PATH_AUTO || path > MOE_PATH_GEMM) return MOE_ERR_ARG;
+  ctx->path = path;
+  return MOE_OK;
+}
+
+int moe_set_router(moe_ctx* ctx, int router) {
+  if (!ctx || router < MOE_ROUTER_AUTO || router > MOE_ROUTER_TENSOR) return MOE_ERR_ARG;
+  ctx->router = router;
+  return MOE_OK;
+}
+
+int moe_set_spin_limit(moe_ctx* ctx, long long limit) {
+  if (!ctx || limit < 0) return MOE_ERR_ARG;
+  ctx->spin_ns = limit == 0 ? kDefaultSpinNs : limit;
+  return MOE_OK;
+}
+
+int moe_time_kernel(moe_ctx* ctx, int kernel_id, void* ev_start, void* ev_stop) {
+  if (!ctx || kernel_id < MOE_K_ROUTER || kernel_id > MOE_K_COMBINE || !ev_start || !ev_stop) return MOE_ERR_ARG;
+  ctx->timed_kernel = kernel_id;
+  ctx->ev_start = static_cast<cudaEvent_t>(ev_start);
+  ctx->ev_stop = static_cast<cudaEvent_t>(ev_stop);
+  return MOE_OK;
+}
+
+long long moe_launch_count(moe_ctx* ctx) { return ctx ? ctx->launches : 0; }
+
+int moe_route(moe_ctx* ctx, const void* x, int T, const float* router_w, const float* router_b, int top_k,
+              int32_t* idx, float* w, int32_t* counts, int32_t* offsets, int32_t* perm, void* stream) {
+  int rc = check_route_args(ctx, x, T, router_w, router_b, top_k);
+  if (rc != MOE_OK || T == 0) return rc;
+  if (!ctx->cfg.has_router_bias) router_b = nullptr;
+  if ((idx && !aligned16(idx)) || (w && !aligned16(w)) || (counts && !aligned16(counts)) ||
+      (offsets && !aligned16(offsets)) || (perm && !aligned16(perm)))
+    return MOE_ERR_ALIGN;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const Shapes s = shapes(ctx, T, top_k);
+  const bool tensor = use_tensor_router(ctx, s);
+  GemmMaps maps;
+  memset(&maps, 0, sizeof(maps));
+  if (tensor) {
+    if ((rc = make_map(ctx, &maps.x_tile, x, s.d, s.T, 64, 128)) != MOE_OK) return rc;
+    if ((rc = make_map(ctx, &maps.wr_split, ctx->sc.wr_split, s.d, 3 * s.E, 64, 128)) != MOE_OK) return rc;
+  }
+  if ((rc = run_route(ctx, s, x, router_w, router_b, tensor, &maps, st)) != MOE_OK) return rc;
+  return cuda_fail(launch_export_route(s, ctx->sc, idx, w, counts, offsets, perm, st));
+}
+
+int moe_forward(moe_ctx* ctx, const void* x, int T, const float* router_w, const float* router_b,
+                const void* experts_gate_up, const void* experts_down, const void* shared_w, int top_k, void* y,
+                void* stream) {
+  int rc = check_route_args(ctx, x, T, router_w, router_b, top_k);
+  if (rc != MOE_OK || T == 0) return rc;
+  const moe_config& c = ctx->cfg;
+  if (!experts_gate_up || !experts_down || !y || (c.has_shared && !shared_w)) return MOE_ERR_ARG;
+  if (!aligned16(experts_gate_up) || !aligned16(experts_down) || !aligned16(y) ||
+      (shared_w && !aligned16(shared_w)))
+    return MOE_ERR_ALIGN;
+  if (!c.has_router_bias) router_b = nullptr;
+  if (!c.has_shared) shared_w = nullptr;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const Shapes s = shapes(ctx, T, top_k);
+  int path = ctx->path;
+  if (path == MOE_PATH_AUTO) path = (T <= kGemvMaxT && T <= ctx->gemv_max_t) ? MOE_PATH_GEMV : MOE_PATH_GEMM;
+  if (path == MOE_PATH_GEMV && T > ctx->gemv_max_t) return MOE_ERR_UNSUPPORTED;
+  const DevCtl ctl = devctl(ctx);
+  const uint16_t* gu = static_cast<const uint16_t*>(experts_gate_up);
+  const uint16_t* dn = static_cast<const uint16_t*>(experts_down);
+  const uint16_t* sw = static_cast<const uint16_t*>(shared_w);
+
+  if (path == MOE_PATH_GEMV) {
+    if ((rc = run_route(ctx, s, x, router_w, router_b, false, nullptr, st)) != MOE_OK) return rc;
+    const Scratch& sc = ctx->sc;
+    const int sms = ctx->num_sms;
+    cudaError_t err =
+        launch(ctx, MOE_K_GEMV_GATE_UP, st, [&] { return launch_gemv_gate_up(s, x, gu, sw, sc, ctl, sms, st); });
+    if (err == cudaSuccess)
+      err = launch(ctx, MOE_K_GEMV_DOWN, st, [&] { return launch_gemv_down(s, dn, sw, y, sc, ctl, sms, st); });
+    return cuda_fail(err);
+  }
+
+  // grouped-GEMM path
+  const bool tensor = use_tensor_router(ctx, s);
+  const void* xb = x;
+  if (!s.x_bf16) {
+    cudaError_t err =
+        launch(ctx, -3, st, [&] { return launch_x_to_bf16(s, static_cast<const float*>(x), ctx->sc, st); });
+    if (err != cudaSuccess) return MOE_ERR_CUDA;
+    xb = ctx->sc.x_bf16;
+  }
+  GemmMaps maps;
+  memset(&maps, 0, sizeof(maps));
+  const uint64_t rows = (uint64_t)s.T * s.k + (s.has_shared ? s.T : 0);
+  if ((rc = make_map(ctx, &maps.x_rows, xb, s.d, s.T, 64, 1)) != MOE_OK) return rc;
+  if ((rc = make_map(ctx, &maps.x_tile, xb, s.d, s.T, 64, 128)) != MOE_OK) return rc;
+  if ((rc = make_map(ctx, &maps.gate_up, gu, s.d, (uint64_t)s.E * 2 * s.I, 64, 128)) != MOE_OK) return rc;
+  if ((rc = make_map(ctx, &maps.h, ctx->sc.h, s.I, rows, 64, 128)) != MOE_OK) return rc;
+  if ((rc = make_map(ctx, &maps.down, dn, s.I, (uint64_t)s.E * s.d, 64, 256)) != MOE_OK) return rc;
+  if ((rc = make_map(ctx, &maps.wr_split, ctx->sc.wr_split, s.d, 3 * s.E, 64, 128)) != MOE_OK) return rc;
+  // without a shared expert these maps are never read; point them at routed weights
+  const uint16_t* sgu = sw ? sw : gu;
+  const uint16_t* sdn = sw ? sw + (size_t)2 * s.I * s.d : dn;
+  if ((rc = make_map(ctx, &maps.shared_gu, sgu, s.d, 2 * s.I, 64, 128)) != MOE_OK) return rc;
+  if ((rc = make_map(ctx, &maps.shared_down, sdn, s.I, s.d, 64, 256)) != MOE_OK) return rc;
+
+  if ((rc = run_route(ctx, s, x, router_w, router_b, tensor, &maps, st)) != MOE_OK) return rc;
+  const Scratch& sc = ctx->sc;
+  const int sms = ctx->num_sms;
+  cudaError_t err =
+      launch(ctx, MOE_K_GEMM_GATE_UP, st, [&] { return launch_gemm_gate_up(s, maps, sc, ctl, sms, st); });
+  if (err == cudaSuccess)
+    err = launch(ctx, MOE_K_GEMM_DOWN, st, [&] { return launch_gemm_down(s, maps, sc, ctl, sms, st); });
+  if (err == cudaSuccess) err = launch(ctx, MOE_K_COMBINE, st, [&] { return launch_combine(s, y, sc, st); });
+  return cuda_fail(err);
+}
+
+int moe_status(moe_ctx* ctx) {
+  if (!ctx) return MOE_ERR_ARG;
+  if (cudaDeviceSynchronize() != cudaSuccess) return MOE_ERR_CUDA;
+  unsigned v = 0;
+  if (cudaMemcpy(&v, ctx->sc.status, 4, cudaMemcpyDeviceToHost) != cudaSuccess) return MOE_ERR_CUDA;
+  if (v && cudaMemset(ctx->sc.status, 0, 4) != cudaSuccess) return MOE_ERR_CUDA;
+  if (v & kStatusTimeout) return MOE_ERR_TIMEOUT;
+  if (v & kStatusBounds) return MOE_ERR_BOUNDS;
+  return MOE_OK;
+}
+
+void moe_destroy(moe_ctx* ctx) {
+  if (!ctx) return;
+  cudaDeviceSynchronize();
+  if (ctx->block) cudaFree(ctx->block);
+  delete ctx;
+}
+
+}  // extern "C"

@@ -1,0 +1,84 @@
+// Weighted combine of the grouped-GEMM path, and the fp32 -> bf16 copy of x
+// that feeds the tensor cores when x is stored in fp32.
+//
+// "Optimizing on-device inference for Apple Silicon", section "Reducing
+// intermediate and state traffic": the experts' output projections are
+// combined with their routing scores and the shared expert's result.  Here,
+// per token t: y_t = sum_j w[t, j] * out[slot[t, j]] + out[T*k + t], summed in
+// fp32 over j in ascending expert order, then stored in x's dtype.
+#include "moe_internal.h"
+
+namespace moe {
+
+__global__ void x_to_bf16_kernel(size_t n, const float* __restrict__ x, uint16_t* __restrict__ out) {
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n / 2; i += (size_t)gridDim.x * blockDim.x) {
+    const float2 v = reinterpret_cast<const float2*>(x)[i];
+    reinterpret_cast<uint32_t*>(out)[i] = pack_bf16x2(v.x, v.y);
+  }
+}
+
+cudaError_t launch_x_to_bf16(const Shapes& s, const float* x, const Scratch& sc, cudaStream_t st) {
+  const size_t n = (size_t)s.T * s.d;
+  const size_t want = (n / 2 + 255) / 256;
+  const int blocks = (int)(want < 4096 ? want : 4096);
+  x_to_bf16_kernel<<<blocks, 256, 0, st>>>(n, x, sc.x_bf16);
+  return cudaGetLastError();
+}
+
+// One warp per (token, 256-column slice); each lane owns 8 consecutive columns
+// and reads them with one 16-byte load per contributing row.
+template <bool YBF16>
+__global__ void __launch_bounds__(256) combine_kernel(Shapes s, void* __restrict__ y, Scratch sc) {
+  const int lane = threadIdx.x & 31;
+  const int slices = s.d >> 8;
+  const long long gw = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
+  if (gw >= (long long)s.T * slices) return;
+  const int t = (int)(gw / slices);
+  const int col = (int)(gw - (long long)t * slices) * 256 + lane * 8;
+  float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  for (int j = 0; j < s.k; ++j) {
+    const int p = sc.slot[(size_t)t * s.k + j];
+    const float wj = sc.w[(size_t)t * s.k + j];
+    const uint4 v = __ldcs(reinterpret_cast<const uint4*>(sc.out + (size_t)p * s.d + col));
+    acc[0] = fmaf(wj, bf16_lo(v.x), acc[0]);
+    acc[1] = fmaf(wj, bf16_hi(v.x), acc[1]);
+    acc[2] = fmaf(wj, bf16_lo(v.y), acc[2]);
+    acc[3] = fmaf(wj, bf16_hi(v.y), acc[3]);
+    acc[4] = fmaf(wj, bf16_lo(v.z), acc[4]);
+    acc[5] = fmaf(wj, bf16_hi(v.z), acc[5]);
+    acc[6] = fmaf(wj, bf16_lo(v.w), acc[6]);
+    acc[7] = fmaf(wj, bf16_hi(v.w), acc[7]);
+  }
+  if (s.has_shared) {
+    const uint4 v = __ldcs(reinterpret_cast<const uint4*>(sc.out + ((size_t)s.T * s.k + t) * s.d + col));
+    acc[0] += bf16_lo(v.x);
+    acc[1] += bf16_hi(v.x);
+    acc[2] += bf16_lo(v.y);
+    acc[3] += bf16_hi(v.y);
+    acc[4] += bf16_lo(v.z);
+    acc[5] += bf16_hi(v.z);
+    acc[6] += bf16_lo(v.w);
+    acc[7] += bf16_hi(v.w);
+  }
+  if (YBF16) {
+    uint4 o = make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]), pack_bf16x2(acc[4], acc[5]),
+                         pack_bf16x2(acc[6], acc[7]));
+    *reinterpret_cast<uint4*>(static_cast<uint16_t*>(y) + (size_t)t * s.d + col) = o;
+  } else {
+    float4* o = reinterpret_cast<float4*>(static_cast<float*>(y) + (size_t)t * s.d + col);
+    o[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+    o[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+  }
+}
+
+cudaError_t launch_combine(const Shapes& s, void* y, const Scratch& sc, cudaStream_t st) {
+  const long long warps = (long long)s.T * (s.d >> 8);
+  const int blocks = (int)((warps + 7) / 8);
+  if (s.x_bf16)
+    combine_kernel<true><<<blocks, 256, 0, st>>>(s, y, sc);
+  else
+    combine_kernel<false><<<blocks, 256, 0, st>>>(s, y, sc);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

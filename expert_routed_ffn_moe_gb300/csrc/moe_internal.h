@@ -1,0 +1,98 @@
+// Internal declarations shared by the translation units of the MoE library:
+// the layout of a context's scratch memory and the kernel launchers.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "moe.h"
+#include "moe_common.cuh"
+
+namespace moe {
+
+constexpr int kMaxExperts = 256;
+constexpr int kMaxTopK = 32;
+constexpr int kChunk = 32;       // tokens per grouping chunk (one bit each in a 32-bit mask)
+constexpr int kBM = 128;         // rows (tokens) per grouped-GEMM tile
+constexpr int kGemvMaxT = 8;     // largest T the automatic path sends to the GEMV kernels
+
+// m-tile of the grouped GEMM: rows [row0, row0 + rows) of the expert-grouped
+// buffers belong to expert `e` (e == E is the shared expert).
+struct MTile {
+  int e, row0, rows, pad;
+};
+
+// Device scratch memory of one context (all sized for max_tokens).
+struct Scratch {
+  float* logits;          // [T, E] fp32 router logits (SIMT router) / [3, T, E] partials (tensor router)
+  int* idx;               // [T, k]
+  float* w;               // [T, k]
+  unsigned* chunk_mask;   // [nchunk, E]: bit i = token chunk*32+i chose expert e
+  int* chunk_base;        // [E, nchunk]: per-chunk count, then the exclusive prefix within expert
+  int* counts;            // [E + 1]; counts[E] = T for the shared expert
+  int* offsets;           // [E + 2]; offsets[E] = T*k, offsets[E+1] = T*k + T
+  int* perm;              // [T*k + T]: token of each grouped row; rows T*k.. are the shared expert's
+  int* slot;              // [T, k]: grouped row of (t, idx[t][j])
+  MTile* mtiles;          // grouped-GEMM m-tiles
+  int* meta;              // [0] = number of m-tiles, [1] = number of active experts
+  int* active;            // [E + 1]: experts with count > 0, ascending, then the shared expert
+  unsigned* tickets;      // last-block counters (self-resetting)
+  uint16_t* x_bf16;       // [T, d] bf16 copy of an fp32 x (GEMM path)
+  uint16_t* wr_split;     // [3E, d] router weights as bf16 hi + mid + lo terms
+  uint16_t* h;            // [T*k + T, I] bf16 SwiGLU activations, grouped rows (GEMM path)
+  float* h_gemv;          // [Tg*k + Tg, I] fp32 SwiGLU activations (GEMV path)
+  uint16_t* out;          // [T*k + T, d] bf16 expert outputs, grouped rows (GEMM path)
+  unsigned* status;       // device status word
+  int max_mtiles;
+};
+
+struct Shapes {
+  int T, d, E, I, k;
+  int has_shared;
+  int x_bf16;             // 1: x is bf16, 0: fp32
+};
+
+// moe_route.cu
+cudaError_t launch_router_logits_simt(const Shapes& s, const void* x, const float* wr, const float* rb,
+                                      const Scratch& sc, cudaStream_t st);
+cudaError_t launch_router_split_weights(const Shapes& s, const float* wr, const Scratch& sc, cudaStream_t st);
+cudaError_t launch_select(const Shapes& s, const float* rb, int logit_parts, const Scratch& sc,
+                          const DevCtl& ctl, cudaStream_t st);
+cudaError_t launch_group(const Shapes& s, const Scratch& sc, const DevCtl& ctl, cudaStream_t st);
+cudaError_t launch_export_route(const Shapes& s, const Scratch& sc, int32_t* idx, float* w, int32_t* counts,
+                                int32_t* offsets, int32_t* perm, cudaStream_t st);
+
+// moe_gemv.cu
+size_t gemv_gate_up_smem(const Shapes& s);
+size_t gemv_down_smem(const Shapes& s);
+cudaError_t launch_gemv_gate_up(const Shapes& s, const void* x, const uint16_t* gate_up, const uint16_t* shared_w,
+                                const Scratch& sc, const DevCtl& ctl, int num_sms, cudaStream_t st);
+cudaError_t prepare_gemv_kernels(int max_smem);
+cudaError_t launch_gemv_down(const Shapes& s, const uint16_t* down, const uint16_t* shared_w, void* y,
+                             const Scratch& sc, const DevCtl& ctl, int num_sms, cudaStream_t st);
+
+// moe_gemm.cu
+struct GemmMaps {
+  CUtensorMap x_rows;       // x (bf16) [T, d], box 64 x 1 (row gather)
+  CUtensorMap x_tile;       // x (bf16) [T, d], box 64 x 128
+  CUtensorMap gate_up;      // experts [E*2I, d], box 64 x 128
+  CUtensorMap shared_gu;    // shared gate_up [2I, d], box 64 x 128
+  CUtensorMap h;            // h [T*k + T, I], box 64 x 128
+  CUtensorMap down;         // experts [E*d, I], box 64 x 256
+  CUtensorMap shared_down;  // shared down [d, I], box 64 x 256
+  CUtensorMap wr_split;     // router weights hi/mid/lo [3E, d], box 64 x 128
+};
+cudaError_t prepare_gemm_kernels();
+cudaError_t launch_gemm_gate_up(const Shapes& s, const GemmMaps& m, const Scratch& sc, const DevCtl& ctl,
+                                int num_sms, cudaStream_t st);
+cudaError_t launch_gemm_down(const Shapes& s, const GemmMaps& m, const Scratch& sc, const DevCtl& ctl,
+                             int num_sms, cudaStream_t st);
+cudaError_t launch_gemm_router(const Shapes& s, const GemmMaps& m, const Scratch& sc, const DevCtl& ctl,
+                               int num_sms, cudaStream_t st);
+
+// moe_combine.cu
+cudaError_t launch_x_to_bf16(const Shapes& s, const float* x, const Scratch& sc, cudaStream_t st);
+cudaError_t launch_combine(const Shapes& s, void* y, const Scratch& sc, cudaStream_t st);
+
+}  // namespace moe

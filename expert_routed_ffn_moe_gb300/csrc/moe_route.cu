@@ -1,0 +1,423 @@
+// Routing: router logits, top-k selection with renormalised weights, and the
+// GPU-resident grouping of tokens by expert (histogram, exclusive prefix,
+// stable scatter, and the list of grouped-GEMM tiles).
+//
+// "Optimizing on-device inference for Apple Silicon", section "Qwen creates
+// three different workload shapes": the router scores 256 experts per token
+// and keeps eight.  Section "Keeping expert routing on the GPU": a histogram
+// counts the assignments of each expert, a prefix pass turns the counts into
+// start offsets, a scatter places the rows into their expert groups, and a
+// block map lists the fixed-size tiles the grouped GEMM must process -- all
+// inside one command stream, without a CPU round trip.
+//
+// Grouping here is deterministic: tokens are cut into chunks of 32; each chunk
+// records, per expert, a 32-bit mask of the tokens that chose it.  The rank of
+// token t inside its expert group is then (offset of the expert) + (tokens of
+// the expert in earlier chunks) + popc(mask & bits below t), which yields the
+// stable (expert asc, token asc) order without atomics deciding any position.
+#include <float.h>
+#include <math.h>
+
+#include "moe_internal.h"
+
+namespace moe {
+
+// ----------------------------------------------------------- router logits
+// Small T: one warp per (expert, group of up to 16 tokens); the expert's row
+// of router_w is streamed once per group with 16-byte loads.
+template <bool XBF16>
+__global__ void __launch_bounds__(256) router_logits_small_kernel(Shapes s, const void* __restrict__ x,
+                                                                   const float* __restrict__ wr,
+                                                                   float* __restrict__ logits) {
+  const int lane = threadIdx.x & 31;
+  const int gw = blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int e = gw % s.E;
+  const int g = gw / s.E;
+  const int t0 = g * 16;
+  if (t0 >= s.T) return;
+  const int nt = min(16, s.T - t0);
+  float acc[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) acc[i] = 0.f;
+  const float4* wrow = reinterpret_cast<const float4*>(wr + (size_t)e * s.d);
+  const int n4 = s.d >> 2;
+#pragma unroll 4
+  for (int c = lane; c < n4; c += 32) {
+    const float4 wv = __ldg(wrow + c);
+#pragma unroll
+    for (int tt = 0; tt < 16; ++tt) {
+      if (tt < nt) {
+        float4 xv;
+        if (XBF16) {
+          const uint2 raw = __ldg(reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(x) +
+                                                                 (size_t)(t0 + tt) * s.d) + c);
+          xv = make_float4(bf16_lo(raw.x), bf16_hi(raw.x), bf16_lo(raw.y), bf16_hi(raw.y));
+        } else {
+          xv = __ldg(reinterpret_cast<const float4*>(static_cast<const float*>(x) + (size_t)(t0 + tt) * s.d) + c);
+        }
+        acc[tt] = fmaf(xv.x, wv.x, acc[tt]);
+        acc[tt] = fmaf(xv.y, wv.y, acc[tt]);
+        acc[tt] = fmaf(xv.z, wv.z, acc[tt]);
+        acc[tt] = fmaf(xv.w, wv.w, acc[tt]);
+      }
+    }
+  }
+#pragma unroll
+  for (int tt = 0; tt < 16; ++tt) {
+    if (tt < nt) {
+      const float r = warp_sum(acc[tt]);
+      if (lane == 0) logits[(size_t)(t0 + tt) * s.E + e] = r;
+    }
+  }
+}
+
+// Larger T: a 64-token x 64-expert tile per block, 16-deep k slices staged in
+// shared memory, 4 x 4 outputs per thread, fp32 FMA.
+template <bool XBF16>
+__global__ void __launch_bounds__(256) router_logits_tiled_kernel(Shapes s, const void* __restrict__ x,
+                                                                   const float* __restrict__ wr,
+                                                                   float* __restrict__ logits) {
+  __shared__ float xs[16][64 + 4];
+  __shared__ float ws[16][64 + 4];
+  const int tid = threadIdx.x;
+  const int t0 = blockIdx.x * 64, e0 = blockIdx.y * 64;
+  const int ty = tid >> 4, tx = tid & 15;
+  float acc[4][4] = {};
+  // loader mapping: row r = tid / 4 (0..63), k quad q = tid % 4 (4 values each)
+  const int lr = tid >> 2, lq = (tid & 3) * 4;
+  for (int k0 = 0; k0 < s.d; k0 += 16) {
+    {
+      const int t = t0 + lr;
+      float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (t < s.T) {
+        if (XBF16) {
+          const uint2 raw = *reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(x) + (size_t)t * s.d + k0 + lq);
+          v = make_float4(bf16_lo(raw.x), bf16_hi(raw.x), bf16_lo(raw.y), bf16_hi(raw.y));
+        } else {
+          v = *reinterpret_cast<const float4*>(static_cast<const float*>(x) + (size_t)t * s.d + k0 + lq);
+        }
+      }
+      xs[lq + 0][lr] = v.x;
+      xs[lq + 1][lr] = v.y;
+      xs[lq + 2][lr] = v.z;
+      xs[lq + 3][lr] = v.w;
+      const int e = e0 + lr;
+      float4 u = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (e < s.E) u = *reinterpret_cast<const float4*>(wr + (size_t)e * s.d + k0 + lq);
+      ws[lq + 0][lr] = u.x;
+      ws[lq + 1][lr] = u.y;
+      ws[lq + 2][lr] = u.z;
+      ws[lq + 3][lr] = u.w;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int kk = 0; kk < 16; ++kk) {
+      const float4 a = *reinterpret_cast<const float4*>(&xs[kk][ty * 4]);
+      const float4 b = *reinterpret_cast<const float4*>(&ws[kk][tx * 4]);
+      const float av[4] = {a.x, a.y, a.z, a.w}, bv[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(av[i], bv[j], acc[i][j]);
+    }
+    __syncthreads();
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int t = t0 + ty * 4 + i;
+    if (t >= s.T) continue;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int e = e0 + tx * 4 + j;
+      if (e < s.E) logits[(size_t)t * s.E + e] = acc[i][j];
+    }
+  }
+}
+
+cudaError_t launch_router_logits_simt(const Shapes& s, const void* x, const float* wr, const float*,
+                                      const Scratch& sc, cudaStream_t st) {
+  if (s.T <= 64) {
+    const int warps = s.E * ((s.T + 15) / 16);
+    const dim3 grid((warps + 7) / 8);
+    if (s.x_bf16)
+      router_logits_small_kernel<true><<<grid, 256, 0, st>>>(s, x, wr, sc.logits);
+    else
+      router_logits_small_kernel<false><<<grid, 256, 0, st>>>(s, x, wr, sc.logits);
+  } else {
+    const dim3 grid((s.T + 63) / 64, (s.E + 63) / 64);
+    if (s.x_bf16)
+      router_logits_tiled_kernel<true><<<grid, 256, 0, st>>>(s, x, wr, sc.logits);
+    else
+      router_logits_tiled_kernel<false><<<grid, 256, 0, st>>>(s, x, wr, sc.logits);
+  }
+  return cudaGetLastError();
+}
+
+// Router weights split into three bf16 terms, hi = bf16(w), mid = bf16(w - hi),
+// lo = bf16(w - hi - mid), stacked as [3E, d].  hi + mid + lo equals w to about
+// 2^-25 relative, and every bf16 x bf16 product is exact in fp32, so bf16 x
+// times the three terms on the tensor cores (fp32 accumulation) reproduces the
+// fp32 logits.
+__global__ void router_split_kernel(int n, const float* __restrict__ wr, uint16_t* __restrict__ out) {
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) {
+    const float v = wr[i];
+    const __nv_bfloat16 hi = __float2bfloat16_rn(v);
+    const float r1 = v - __bfloat162float(hi);
+    const __nv_bfloat16 mid = __float2bfloat16_rn(r1);
+    const __nv_bfloat16 lo = __float2bfloat16_rn(r1 - __bfloat162float(mid));
+    out[i] = *reinterpret_cast<const uint16_t*>(&hi);
+    out[n + i] = *reinterpret_cast<const uint16_t*>(&mid);
+    out[2 * n + i] = *reinterpret_cast<const uint16_t*>(&lo);
+  }
+}
+
+cudaError_t launch_router_split_weights(const Shapes& s, const float* wr, const Scratch& sc, cudaStream_t st) {
+  const int n = s.E * s.d;
+  router_split_kernel<<<(n + 1023) / 1024, 256, 0, st>>>(n, wr, sc.wr_split);
+  return cudaGetLastError();
+}
+
+// ----------------------------------------------------------- selection
+// One block per chunk of 32 tokens, one warp per token at a time.  Each lane
+// holds the logits of experts lane, lane+32, ...; k rounds of a warp arg-max
+// (ties to the lower expert id) pick the experts.  The weights are
+// exp(l_j - l_max) / sum over the picked of exp(l - l_max): the full softmax
+// over all E experts renormalised over the picked ones, with the common
+// denominator cancelled.  The picks are written in ascending expert id, and
+// the chunk's per-expert token masks feed the grouping.
+__global__ void __launch_bounds__(256) select_kernel(Shapes s, const float* __restrict__ rb, int parts,
+                                                     Scratch sc, DevCtl ctl) {
+  __shared__ unsigned mask[kMaxExperts];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int c = blockIdx.x, t0 = c * kChunk;
+  const int nchunk = (s.T + kChunk - 1) / kChunk;
+  for (int e = tid; e < s.E; e += blockDim.x) mask[e] = 0u;
+  __syncthreads();
+  for (int tl = warp; tl < kChunk; tl += 8) {
+    const int t = t0 + tl;
+    if (t >= s.T) break;
+    float v[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int e = lane + 32 * i;
+      float l = -INFINITY;
+      if (e < s.E) {
+        if (parts == 3) {  // tensor-core partial logits of the lo, mid and hi weight terms, small first
+          const size_t te = (size_t)t * s.E + e, part = (size_t)s.T * s.E;
+          l = (sc.logits[2 * part + te] + sc.logits[part + te]) + sc.logits[te];
+        } else {
+          l = sc.logits[(size_t)t * s.E + e];
+        }
+        if (rb) l += rb[e];
+      }
+      v[i] = l;
+    }
+    unsigned taken = 0u;
+    int my_e = 0;
+    float my_v = 0.f;
+    for (int r = 0; r < s.k; ++r) {
+      float bv = -INFINITY;
+      int bi = s.E;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int e = lane + 32 * i;
+        if (e < s.E && !(taken & (1u << i)) && (v[i] > bv || bi == s.E)) {
+          bv = v[i];
+          bi = e;
+        }
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+        const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+        if (oi < s.E && (bi >= s.E || ov > bv || (ov == bv && oi < bi))) {
+          bv = ov;
+          bi = oi;
+        }
+      }
+      if (bi >= s.E) {  // only reachable with NaN logits
+        if (lane == 0) raise_status(ctl, kStatusBounds);
+        bi = r;
+      }
+      if (lane == (bi & 31)) taken |= 1u << (bi >> 5);
+      if (lane == r) {
+        my_e = bi;
+        my_v = bv;
+      }
+    }
+    const float vmax = __shfl_sync(0xffffffffu, my_v, 0);
+    const float ex = lane < s.k ? expf(my_v - vmax) : 0.f;
+    const float den = warp_sum(ex);
+    int rank = 0;
+    for (int q = 0; q < s.k; ++q) {
+      const int oe = __shfl_sync(0xffffffffu, my_e, q);
+      rank += (oe < my_e) ? 1 : 0;
+    }
+    if (lane < s.k) {
+      sc.idx[(size_t)t * s.k + rank] = my_e;
+      sc.w[(size_t)t * s.k + rank] = ex / den;
+      atomicOr(&mask[my_e], 1u << tl);
+    }
+  }
+  __syncthreads();
+  for (int e = tid; e < s.E; e += blockDim.x) {
+    const unsigned m = mask[e];
+    sc.chunk_mask[(size_t)c * s.E + e] = m;
+    sc.chunk_base[(size_t)e * nchunk + c] = __popc(m);
+  }
+}
+
+cudaError_t launch_select(const Shapes& s, const float* rb, int parts, const Scratch& sc, const DevCtl& ctl,
+                          cudaStream_t st) {
+  const int nchunk = (s.T + kChunk - 1) / kChunk;
+  select_kernel<<<nchunk, 256, 0, st>>>(s, rb, parts, sc, ctl);
+  return cudaGetLastError();
+}
+
+// ----------------------------------------------------------- grouping
+// Block-wide exclusive scan of one int per thread (256 threads).
+__device__ int block_exclusive_scan(int v, int* total) {
+  __shared__ int warp_tot[8];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int incl = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int n = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += n;
+  }
+  if (lane == 31) warp_tot[warp] = incl;
+  __syncthreads();
+  int base = 0, all = 0;
+  for (int i = 0; i < 8; ++i) {
+    base += (i < warp) ? warp_tot[i] : 0;
+    all += warp_tot[i];
+  }
+  __syncthreads();
+  *total = all;
+  return base + incl - v;
+}
+
+// Phase 1 (every block): one warp per expert turns the per-chunk counts into
+// exclusive prefixes over chunks and writes the expert's total.
+// Phase 2 (the last block to finish): expert offsets, the shared expert's
+// group, the grouped-GEMM m-tiles and the list of active experts.
+__global__ void __launch_bounds__(256) group_scan_kernel(Shapes s, Scratch sc) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int nchunk = (s.T + kChunk - 1) / kChunk;
+  const int e = blockIdx.x * 8 + warp;
+  if (e < s.E) {
+    int* col = sc.chunk_base + (size_t)e * nchunk;
+    int carry = 0;
+    for (int c0 = 0; c0 < nchunk; c0 += 32) {
+      const int c = c0 + lane;
+      const int v = c < nchunk ? col[c] : 0;
+      int incl = v;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int n = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += n;
+      }
+      if (c < nchunk) col[c] = carry + incl - v;
+      carry += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    if (lane == 0) sc.counts[e] = carry;
+  }
+  __threadfence();
+  __syncthreads();
+  __shared__ int is_last;
+  if (threadIdx.x == 0) is_last = (atomicAdd(&sc.tickets[0], 1u) == gridDim.x - 1);
+  __syncthreads();
+  if (!is_last) return;
+  __threadfence();
+
+  const int tid = threadIdx.x;
+  const int cnt = tid < s.E ? __ldcg(sc.counts + tid) : 0;
+  int total;
+  const int off = block_exclusive_scan(cnt, &total);
+  if (tid < s.E) sc.offsets[tid] = off;
+  const int shared_cnt = s.has_shared ? s.T : 0;
+  if (tid == 0) {
+    sc.offsets[s.E] = total;  // == T * k
+    sc.offsets[s.E + 1] = total + shared_cnt;
+    sc.counts[s.E] = shared_cnt;
+  }
+  const int nm = (cnt + kBM - 1) / kBM;
+  int mt_total;
+  const int mt_off = block_exclusive_scan(nm, &mt_total);
+  for (int i = 0; i < nm; ++i) {
+    MTile m;
+    m.e = tid;
+    m.row0 = off + i * kBM;
+    m.rows = min(kBM, cnt - i * kBM);
+    m.pad = 0;
+    sc.mtiles[mt_off + i] = m;
+  }
+  const int snm = (shared_cnt + kBM - 1) / kBM;
+  for (int i = tid; i < snm; i += blockDim.x) {
+    MTile m;
+    m.e = s.E;
+    m.row0 = total + i * kBM;
+    m.rows = min(kBM, shared_cnt - i * kBM);
+    m.pad = 0;
+    sc.mtiles[mt_total + i] = m;
+  }
+  int n_act;
+  const int apos = block_exclusive_scan(cnt > 0 ? 1 : 0, &n_act);
+  if (cnt > 0) sc.active[apos] = tid;
+  if (tid == 0) {
+    if (s.has_shared) sc.active[n_act] = s.E;
+    sc.meta[0] = mt_total + snm;
+    sc.meta[1] = n_act + (s.has_shared ? 1 : 0);
+    sc.tickets[0] = 0u;  // ready for the next launch
+  }
+}
+
+// One block per chunk: the grouped row of every (token, pick), and the shared
+// expert's identity rows.
+__global__ void __launch_bounds__(256) group_scatter_kernel(Shapes s, Scratch sc, DevCtl ctl) {
+  const int c = blockIdx.x, t0 = c * kChunk;
+  const int nchunk = (s.T + kChunk - 1) / kChunk;
+  for (int p = threadIdx.x; p < kChunk * s.k; p += blockDim.x) {
+    const int tl = p / s.k, j = p - tl * s.k;
+    const int t = t0 + tl;
+    if (t >= s.T) continue;
+    const int e = sc.idx[(size_t)t * s.k + j];
+    if (e < 0 || e >= s.E) {
+      raise_status(ctl, kStatusBounds);
+      continue;
+    }
+    const unsigned m = sc.chunk_mask[(size_t)c * s.E + e];
+    const int pos = sc.offsets[e] + sc.chunk_base[(size_t)e * nchunk + c] + __popc(m & ((1u << tl) - 1u));
+    sc.perm[pos] = t;
+    sc.slot[(size_t)t * s.k + j] = pos;
+  }
+  if (s.has_shared) {
+    const int tl = threadIdx.x;
+    if (tl < kChunk && t0 + tl < s.T) sc.perm[(size_t)s.T * s.k + t0 + tl] = t0 + tl;
+  }
+}
+
+cudaError_t launch_group(const Shapes& s, const Scratch& sc, const DevCtl& ctl, cudaStream_t st) {
+  const int nchunk = (s.T + kChunk - 1) / kChunk;
+  group_scan_kernel<<<(s.E + 7) / 8, 256, 0, st>>>(s, sc);
+  cudaError_t err = cudaGetLastError();
+  if (err != cudaSuccess) return err;
+  group_scatter_kernel<<<nchunk, 256, 0, st>>>(s, sc, ctl);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_export_route(const Shapes& s, const Scratch& sc, int32_t* idx, float* w, int32_t* counts,
+                                int32_t* offsets, int32_t* perm, cudaStream_t st) {
+  const size_t tk = (size_t)s.T * s.k;
+  cudaError_t err = cudaSuccess;
+  if (idx && err == cudaSuccess) err = cudaMemcpyAsync(idx, sc.idx, tk * 4, cudaMemcpyDeviceToDevice, st);
+  if (w && err == cudaSuccess) err = cudaMemcpyAsync(w, sc.w, tk * 4, cudaMemcpyDeviceToDevice, st);
+  if (counts && err == cudaSuccess)
+    err = cudaMemcpyAsync(counts, sc.counts, (size_t)s.E * 4, cudaMemcpyDeviceToDevice, st);
+  if (offsets && err == cudaSuccess)
+    err = cudaMemcpyAsync(offsets, sc.offsets, (size_t)(s.E + 1) * 4, cudaMemcpyDeviceToDevice, st);
+  if (perm && err == cudaSuccess) err = cudaMemcpyAsync(perm, sc.perm, tk * 4, cudaMemcpyDeviceToDevice, st);
+  return err;
+}
+
+}  // namespace moe

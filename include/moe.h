@@ -1,0 +1,172 @@
+/*
+ * moe.h -- C ABI of the GB300 (sm_103a) routed-expert SwiGLU MoE layer.
+ *
+ * The layer (one per call of moe_forward), for every token row x_t of x[T, d]:
+ *   1. router logits  l[t, e] = sum_i x[t, i] * router_w[e, i] (+ router_b[e]),
+ *      computed to fp32 accuracy;
+ *   2. the top_k experts with the largest logits, listed in ascending expert id;
+ *   3. their weights: softmax over all E logits, renormalised over the chosen k;
+ *   4. tokens grouped by expert: per-expert counts, exclusive-prefix offsets, and
+ *      a permutation listing each expert's tokens in ascending token order;
+ *   5. each chosen expert's SwiGLU FFN  o = W_down (silu(W_gate x) * (W_up x)),
+ *      bf16 weights, fp32 accumulation;
+ *   6. y_t = sum_j w[t, j] * o_{e_j}(x_t) + o_shared(x_t), summed in fp32 and
+ *      stored in x's dtype.
+ * Source: "Optimizing on-device inference for Apple Silicon" (Perplexity), section
+ * "Qwen creates three different workload shapes" (a router scores 256 experts,
+ * picks eight, plus one shared expert that processes every token), section
+ * "Keeping expert routing on the GPU" (histogram, prefix pass to start offsets,
+ * scatter into expert groups, block map, all without a CPU round trip), section
+ * "Dequantizing weights during matrix multiplication" (fp32 accumulation, bf16
+ * output) and section "Reducing intermediate and state traffic" (the two expert
+ * input projections fused with the gated activation; the output projection fused
+ * with the routing score and the shared expert's result).
+ *
+ * Conventions shared by every entry point:
+ *  - All tensor pointers are DEVICE pointers owned by the caller; the library
+ *    never frees them.  Row-major, densely packed, 16-byte aligned
+ *    (MOE_ERR_ALIGN otherwise).  bf16 = 16-bit bfloat16 bit patterns.
+ *  - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy default
+ *    stream).  They never synchronise, never copy to the host and never
+ *    allocate: all scratch memory is owned by the context, sized at moe_init
+ *    for cfg->max_tokens.  Two calls on one context must not overlap in time
+ *    (they share that scratch memory); use one context per concurrent stream.
+ *  - Return codes are the MOE_* values below.  Argument errors are detected on
+ *    the host before anything is launched.  Errors detected by a kernel
+ *    (MOE_ERR_TIMEOUT, MOE_ERR_BOUNDS) are latched in a device status word and
+ *    reported by moe_status().
+ *  - T == 0 is a valid call that launches nothing and returns MOE_OK.
+ */
+#ifndef MOE_GB300_H
+#define MOE_GB300_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* return codes */
+#define MOE_OK 0
+#define MOE_ERR_ARG 1          /* null pointer, bad shape, top_k not in [1, min(E, 32)], T > max_tokens */
+#define MOE_ERR_ALIGN 2        /* a tensor pointer is not 16-byte aligned */
+#define MOE_ERR_UNSUPPORTED 3  /* a shape outside what the kernels handle (see moe_init) */
+#define MOE_ERR_CUDA 4         /* a CUDA runtime/driver call failed (launch, allocation, tensor map) */
+#define MOE_ERR_TIMEOUT 5      /* device side: a bounded wait inside a kernel ran out; work abandoned */
+#define MOE_ERR_BOUNDS 6       /* device side: an index read from scratch memory was out of range */
+#define MOE_ERR_NOMEM 7        /* moe_init could not allocate its scratch memory */
+
+/* dtype of x (and of y, which has the same dtype) */
+#define MOE_F32 0
+#define MOE_BF16 1
+
+/* execution path for the expert FFNs (moe_set_path) */
+#define MOE_PATH_AUTO 0        /* small T: GEMV over the selected experts; otherwise grouped GEMM */
+#define MOE_PATH_GEMV 1        /* bandwidth-bound GEMV (only for small T, else MOE_ERR_UNSUPPORTED) */
+#define MOE_PATH_GEMM 2        /* tcgen05/TMEM grouped GEMM */
+
+/* router logit kernel (moe_set_router) */
+#define MOE_ROUTER_AUTO 0      /* tensor-core router for bf16 x, E == 256 and T > 64; else fp32 FMA */
+#define MOE_ROUTER_SIMT 1      /* fp32 FMA on the CUDA cores */
+#define MOE_ROUTER_TENSOR 2    /* tcgen05: bf16 x times router_w split into bf16 hi + mid + lo terms,
+                                  fp32 accumulation (needs bf16 x and E == 256; else fp32 FMA) */
+
+typedef struct moe_config {
+  int d;               /* model width; multiple of 256 */
+  int n_experts;       /* routed experts E, 1..256 */
+  int inter;           /* routed expert inner size I; multiple of 128 */
+  int shared_inter;    /* shared expert inner size; must equal inter when has_shared */
+  int top_k;           /* largest top_k a call will use, 1..min(E, 32) */
+  int max_tokens;      /* largest T a call will use (scratch memory is sized for it) */
+  int x_dtype;         /* MOE_F32 or MOE_BF16 */
+  int has_router_bias; /* 1: calls pass router_b */
+  int has_shared;      /* 1: calls pass shared_w */
+} moe_config;
+
+typedef struct moe_ctx moe_ctx;
+
+/* Validate `cfg`, select the current CUDA device, allocate the context and its
+ * device scratch memory for cfg->max_tokens tokens.  On success *out owns them
+ * until moe_destroy.  Errors: MOE_ERR_ARG (null pointers, non-positive sizes),
+ * MOE_ERR_UNSUPPORTED (d % 256, inter % 128, E > 256, shared_inter != inter,
+ * device is not sm_103), MOE_ERR_NOMEM, MOE_ERR_CUDA.  Synchronous.
+ * The GEMV path additionally needs d % 256 == 0, inter % 256 == 0 and a T small
+ * enough for x and the activations to fit in shared memory. */
+int moe_init(const moe_config* cfg, moe_ctx** out);
+
+/* Steps 1-4 only, for inspection.  Inputs: x [T, d] (cfg->x_dtype), router_w
+ * [E, d] fp32, router_b [E] fp32 (NULL unless cfg->has_router_bias).  Outputs
+ * (caller-owned device buffers): idx [T, top_k] int32 (ascending expert id per
+ * row), w [T, top_k] fp32, counts [E] int32, offsets [E + 1] int32 (exclusive
+ * prefix of counts; offsets[E] = T * top_k), perm [T * top_k] int32 (token ids
+ * grouped by expert, ascending within a group).  Any output may be NULL to skip
+ * it.  Asynchronous on `stream`. */
+int moe_route(moe_ctx* ctx, const void* x, int T, const float* router_w, const float* router_b,
+              int top_k, int32_t* idx, float* w, int32_t* counts, int32_t* offsets, int32_t* perm,
+              void* stream);
+
+/* The whole layer: y [T, d] (cfg->x_dtype) from x [T, d] (cfg->x_dtype),
+ * router_w [E, d] fp32, router_b [E] fp32 or NULL, experts_gate_up [E, 2I, d]
+ * bf16 (per expert: rows 0..I-1 gate projection, rows I..2I-1 up projection),
+ * experts_down [E, d, I] bf16, shared_w (NULL unless cfg->has_shared): one bf16
+ * buffer holding the shared expert's gate_up [2I, d] followed by its down
+ * [d, I].  y must not alias any input.  Asynchronous on `stream`; captures into
+ * a CUDA graph (no host synchronisation, no allocation). */
+int moe_forward(moe_ctx* ctx, const void* x, int T, const float* router_w, const float* router_b,
+                const void* experts_gate_up, const void* experts_down, const void* shared_w,
+                int top_k, void* y, void* stream);
+
+/* Choose the expert-FFN path for later calls (MOE_PATH_*).  Used for paired
+ * A/B measurements of the two paths on the same inputs.  MOE_ERR_ARG on an
+ * unknown value. */
+int moe_set_path(moe_ctx* ctx, int path);
+
+/* Choose the router logit kernel for later calls (MOE_ROUTER_*).  Both give
+ * fp32-accurate logits; used for paired A/B measurements.  MOE_ERR_ARG on an
+ * unknown value. */
+int moe_set_router(moe_ctx* ctx, int router);
+
+/* Synchronise the device, then read and clear the context's device status
+ * word: MOE_OK, or the first MOE_ERR_TIMEOUT / MOE_ERR_BOUNDS latched by a
+ * kernel since the last call; MOE_ERR_CUDA if the synchronisation itself
+ * reported an error. */
+int moe_status(moe_ctx* ctx);
+
+/* Test hook for the bounded waits: how long (nanoseconds of GPU global time)
+ * a kernel polls a barrier before giving up with MOE_ERR_TIMEOUT.  0 restores
+ * the default (1 s).  MOE_ERR_ARG if negative. */
+int moe_set_spin_limit(moe_ctx* ctx, long long limit);
+
+/* Kernel ids for moe_time_kernel. */
+#define MOE_K_ROUTER 0         /* router logits (fp32 FMA or tensor-core) */
+#define MOE_K_SELECT 1         /* top-k selection and weights */
+#define MOE_K_GROUP 2          /* prefix over chunks/experts and the stable scatter */
+#define MOE_K_GEMV_GATE_UP 3   /* GEMV path: gate/up projections + SwiGLU */
+#define MOE_K_GEMV_DOWN 4      /* GEMV path: down projection + weighted combine + shared */
+#define MOE_K_GEMM_GATE_UP 5   /* grouped GEMM: gate/up projections + SwiGLU */
+#define MOE_K_GEMM_DOWN 6      /* grouped GEMM: down projection */
+#define MOE_K_COMBINE 7        /* grouped-GEMM path: weighted combine + shared */
+
+/* Profiling hook: the next moe_forward/moe_route call on `ctx` records the
+ * CUDA events `ev_start` / `ev_stop` (cudaEvent_t, created by the caller with
+ * timing enabled) on its stream immediately before and after launching kernel
+ * `kernel_id` (MOE_K_*), then disarms.  Works under stream capture (the
+ * records become graph nodes).  If that call does not launch the kernel the
+ * events are not recorded.  MOE_ERR_ARG on a bad id or null event. */
+int moe_time_kernel(moe_ctx* ctx, int kernel_id, void* ev_start, void* ev_stop);
+
+/* Number of kernels this context has launched (or captured) so far. */
+long long moe_launch_count(moe_ctx* ctx);
+
+/* Static description of a return code. */
+const char* moe_strerror(int code);
+
+/* Free the context and its scratch memory (synchronises the device first).
+ * NULL is a no-op. */
+void moe_destroy(moe_ctx* ctx);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_GB300_H */

@@ -1,0 +1,61 @@
+"""The C ABI library builds, loads and exports every function include/moe.h
+declares; host-side argument checks answer without touching a GPU."""
+import ctypes
+
+import pytest
+
+import expert_routed_ffn_moe_gb300 as moe
+
+
+@pytest.fixture(scope="module")
+def lib():
+    moe.build()
+    return moe.lib()
+
+
+def test_every_declared_function_is_exported(lib):
+    names = moe.header_functions()
+    assert {"moe_init", "moe_route", "moe_forward", "moe_status", "moe_strerror", "moe_destroy"} <= set(names)
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_strerror_covers_codes(lib):
+    seen = {moe.moe_strerror(c) for c in range(8)}
+    assert len(seen) == 8 and moe.moe_strerror(99) == "unknown error"
+
+
+def _cfg(**kw):
+    base = dict(d=512, n_experts=256, inter=128, shared_inter=128, top_k=8, max_tokens=32, x_dtype=moe.MOE_F32,
+                has_router_bias=0, has_shared=1)
+    base.update(kw)
+    return moe.moe_config(**base)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(d=0), moe.MOE_ERR_ARG),
+    (dict(top_k=0), moe.MOE_ERR_ARG),
+    (dict(top_k=33, n_experts=256), moe.MOE_ERR_ARG),
+    (dict(top_k=9, n_experts=8), moe.MOE_ERR_ARG),
+    (dict(max_tokens=0), moe.MOE_ERR_ARG),
+    (dict(x_dtype=7), moe.MOE_ERR_ARG),
+    (dict(d=500), moe.MOE_ERR_UNSUPPORTED),
+    (dict(inter=100, shared_inter=100), moe.MOE_ERR_UNSUPPORTED),
+    (dict(n_experts=300), moe.MOE_ERR_UNSUPPORTED),
+    (dict(shared_inter=256), moe.MOE_ERR_UNSUPPORTED),
+])
+def test_init_rejects_bad_configs_before_any_device_call(lib, kw, code):
+    h = ctypes.c_void_p()
+    assert lib.moe_init(ctypes.byref(_cfg(**kw)), ctypes.byref(h)) == code
+    assert not h.value
+
+
+def test_null_arguments(lib):
+    h = ctypes.c_void_p()
+    assert lib.moe_init(None, ctypes.byref(h)) == moe.MOE_ERR_ARG
+    assert lib.moe_init(ctypes.byref(_cfg()), None) == moe.MOE_ERR_ARG
+    assert lib.moe_forward(None, None, 1, None, None, None, None, None, 8, None, None) == moe.MOE_ERR_ARG
+    assert lib.moe_route(None, None, 1, None, None, 8, None, None, None, None, None, None) == moe.MOE_ERR_ARG
+    assert lib.moe_set_path(None, 0) == moe.MOE_ERR_ARG
+    assert lib.moe_status(None) == moe.MOE_ERR_ARG
+    lib.moe_destroy(None)

@@ -1,0 +1,197 @@
+"""GPU path vs the fp64 oracle, through the C ABI, on the seeded workloads.
+
+Routing (indices, counts, offsets, permutation) must match bit for bit and y
+must be within relative L2 1e-2 / max-abs 2e-2 (tests/moe_case.py).  Full-size
+workloads compare routing for every token and y on a sample of tokens that the
+oracle computes one by one; small ones compare every token.
+"""
+import dataclasses
+
+import numpy as np
+import pytest
+import torch
+
+import moe_workloads as mw
+import expert_routed_ffn_moe_gb300 as moe
+from moe_case import (check_routing, check_y, device_inputs, gpu_run, layer_inputs, make_layer, oracle_routing,
+                      oracle_y, sample_tokens, y_host)
+
+pytestmark = pytest.mark.gpu
+
+W = mw.WORKLOADS
+
+
+def custom(name, **kw):
+    base = dict(T=64, d=512, E=64, I=256, I_s=256, k=4, cid=90)
+    base.update(kw)
+    return mw.Workload(name, **base)
+
+
+def full_case(w, layer_id=0, path=moe.MOE_PATH_AUTO, router=moe.MOE_ROUTER_AUTO, n_sample=64, inp=None):
+    inp = inp or layer_inputs(w, layer_id)
+    layer = make_layer(w, path=path, router=router)
+    got, y = gpu_run(w, inp, layer)
+    layer.close()
+    ref = oracle_routing(w, inp)
+    check_routing(got, ref)
+    toks = sample_tokens(w.T, n_sample)
+    return check_y(y_host(y)[toks], oracle_y(w, inp, toks), f"{w.name} layer {layer_id}")
+
+
+# ------------------------------------------------------------ the workloads
+
+def test_tiny_fp32_x():
+    full_case(W["tiny"])
+
+
+@pytest.mark.parametrize("layer_id", [0, 7])
+def test_decode_layer(layer_id):
+    full_case(W["decode"], layer_id)
+
+
+def test_decode_on_grouped_gemm_path():
+    full_case(W["decode"], 3, path=moe.MOE_PATH_GEMM)
+
+
+@pytest.mark.parametrize("name", ["sweep_T2", "sweep_T8", "sweep_T32", "sweep_T128"])
+def test_sweep_small(name):
+    full_case(W[name])
+
+
+def test_prefill_balanced():
+    full_case(W["prefill_balanced"], n_sample=48)
+
+
+def test_prefill_skewed():
+    full_case(W["prefill_skewed"], n_sample=48)
+
+
+def test_long_prefill_32768():
+    full_case(W["sweep_T32768"], n_sample=24)
+
+
+def test_prefill_simt_router_matches():
+    full_case(W["prefill_balanced"], router=moe.MOE_ROUTER_SIMT, n_sample=16)
+
+
+# ------------------------------------------------------------ edge cases
+
+@pytest.mark.parametrize("T", [1, 31, 33, 129, 300, 1000])
+def test_ragged_token_counts(T):
+    full_case(custom(f"ragged{T}", T=T))
+
+
+def test_gemv_and_gemm_paths_agree_fp32_x():
+    w = custom("gemv_f32", T=8, x_dtype="f32")
+    inp = layer_inputs(w)
+    a = full_case(w, path=moe.MOE_PATH_GEMV, inp=inp)
+    b = full_case(w, path=moe.MOE_PATH_GEMM, inp=inp)
+    assert a[0] < 1e-2 and b[0] < 1e-2
+
+
+@pytest.mark.parametrize("path", [moe.MOE_PATH_GEMV, moe.MOE_PATH_GEMM])
+def test_no_shared_expert(path):
+    full_case(custom("noshared", T=8, I_s=0), path=path)
+
+
+def test_router_bias_small():
+    full_case(custom("bias", T=200, skewed=True))
+
+
+def test_single_expert_is_dense_ffn():
+    full_case(custom("dense", T=100, E=1, k=1, I_s=0))
+
+
+def test_top_k_below_configured():
+    w = custom("k2", T=150, k=8)
+    inp = layer_inputs(dataclasses.replace(w, k=2))
+    w2 = dataclasses.replace(w, k=2)
+    layer = make_layer(w)  # configured for top-8, called with top-2
+    got, y = gpu_run(w2, inp, layer, top_k=2)
+    layer.close()
+    check_routing(got, oracle_routing(w2, inp))
+    toks = sample_tokens(w.T, 40)
+    check_y(y_host(y)[toks], oracle_y(w2, inp, toks), "top-2")
+
+
+def test_many_experts_per_token():
+    full_case(custom("k32", T=40, E=64, k=32))
+
+
+def test_zero_tokens_is_a_noop():
+    w = custom("zero", T=4)
+    layer = make_layer(w)
+    d = device_inputs(w, layer_inputs(w))
+    y = torch.full_like(d["x"], 7.0)
+    moe.moe_forward(layer.ctx, d["x"][:0], d["router_w"], d["router_b"], d["gate_up"], d["down"], d["shared"],
+                    w.k, y[:0])
+    torch.cuda.synchronize()
+    assert layer.status() == moe.MOE_OK and bool((y == 7.0).all())
+    layer.close()
+
+
+# ------------------------------------------------------------ properties
+
+def test_deterministic_and_token_permutation_equivariant():
+    w = custom("equiv", T=300, d=1024, E=128, I=256, k=8)
+    inp = layer_inputs(w)
+    layer = make_layer(w)
+    d = device_inputs(w, inp)
+    args = (d["router_w"], d["router_b"], d["gate_up"], d["down"], d["shared"])
+    y1 = layer.forward(d["x"], *args).clone()
+    y2 = layer.forward(d["x"], *args).clone()
+    p = torch.from_numpy(np.random.default_rng(5).permutation(w.T)).cuda()
+    yp = layer.forward(d["x"][p].contiguous(), *args).clone()
+    torch.cuda.synchronize()
+    assert layer.status() == moe.MOE_OK
+    layer.close()
+    assert torch.equal(y1, y2), "two runs differ"
+    assert torch.equal(yp, y1[p]), "not equivariant under token permutation"
+
+
+# ------------------------------------------------------------ errors
+
+def test_argument_errors():
+    w = custom("errs", T=16)
+    layer = make_layer(w)
+    d = device_inputs(w, layer_inputs(w))
+    y = torch.empty_like(d["x"])
+    base = [d["router_w"], d["router_b"], d["gate_up"], d["down"], d["shared"]]
+    with pytest.raises(moe.MoeError) as e:
+        moe.moe_forward(layer.ctx, d["x"], *base, 0, y)
+    assert e.value.code == moe.MOE_ERR_ARG
+    with pytest.raises(moe.MoeError) as e:
+        moe.moe_forward(layer.ctx, d["x"], *base, w.k + 1, y)
+    assert e.value.code == moe.MOE_ERR_ARG
+    big = torch.cat([d["x"], d["x"]])
+    with pytest.raises(moe.MoeError) as e:
+        moe.moe_forward(layer.ctx, big, *base, w.k, torch.empty_like(big))
+    assert e.value.code == moe.MOE_ERR_ARG
+    flat = torch.empty(d["x"].numel() + 8, dtype=d["x"].dtype, device="cuda")
+    xm = flat[1:1 + d["x"].numel()].view_as(d["x"])  # 2-byte offset: not 16-byte aligned
+    with pytest.raises(moe.MoeError) as e:
+        moe.moe_forward(layer.ctx, xm, *base, w.k, y)
+    assert e.value.code == moe.MOE_ERR_ALIGN
+    assert moe.lib().moe_forward(layer.ctx, None, 4, None, None, None, None, None, w.k, None, None) == moe.MOE_ERR_ARG
+    layer.close()
+
+
+def test_bounded_wait_reports_timeout_and_context_recovers():
+    # A 1 ns limit makes the first barrier wait that is not already complete
+    # give up: the grouped GEMM must return with MOE_ERR_TIMEOUT latched (no
+    # trap, no hang), and the same context must then run correctly again.
+    w = custom("timeout", T=256)
+    inp = layer_inputs(w)
+    layer = make_layer(w, path=moe.MOE_PATH_GEMM)
+    d = device_inputs(w, inp)
+    args = (d["router_w"], d["router_b"], d["gate_up"], d["down"], d["shared"])
+    moe.moe_set_spin_limit(layer.ctx, 1)
+    layer.forward(d["x"], *args)
+    assert layer.status() == moe.MOE_ERR_TIMEOUT
+    moe.moe_set_spin_limit(layer.ctx, 0)
+    y = layer.forward(d["x"], *args)
+    torch.cuda.synchronize()
+    assert layer.status() == moe.MOE_OK
+    layer.close()
+    toks = sample_tokens(w.T, 32)
+    check_y(y_host(y)[toks], oracle_y(w, inp, toks), "after timeout")
