@@ -169,42 +169,77 @@ def layer_costs(w: mw.Workload, idx: np.ndarray):
 
 
 def dominant_kernel(path: int):
+    """The kernel whose roofline the bench line reports: for the small-T path
+    the fused decode kernel is the whole layer; for the grouped-GEMM path the
+    gate/up GEMM moves two thirds of the expert bytes."""
     import expert_routed_ffn_moe_gb300 as moe
 
-    return moe.MOE_K_GEMV_GATE_UP if path == moe.MOE_PATH_GEMV else moe.MOE_K_GEMM_GATE_UP
+    return moe.MOE_K_DECODE_FUSED if path == moe.MOE_PATH_GEMV else moe.MOE_K_GEMM_GATE_UP
 
 
 # ------------------------------------------------------------------ oracle leg
-def oracle_sample(w: mw.Workload, budget_s: float, host_inputs, seed=0):
-    """Time the fp64 oracle on a bounded sample of tokens; returns (tokens/s, tokens, seconds, threads)."""
+def oracle_sample(w: mw.Workload, budget_s: float, host_inputs):
+    """Time the fp64 oracle on a bounded sample of tokens; returns (tokens/s, tokens, seconds, threads).
+
+    Each host input holds the tokens to evaluate and exactly the experts the
+    oracle's own routing of those tokens selects (see ``host_layer_for_oracle``)."""
     import oracle
 
     threads = int(os.environ.get("OPENBLAS_NUM_THREADS", os.cpu_count() or 1))
-    rng = np.random.default_rng(seed)
     done, t0 = 0, time.perf_counter()
     while True:
-        for layer, inp in enumerate(host_inputs):
-            n = min(w.T, 8)
-            toks = np.sort(rng.choice(w.T, n, replace=False))
+        for inp in host_inputs:
             oracle.moe_layer(inp["x"], inp["router_w"], inp["router_b"], inp["gate_up"], inp["down"], inp["shared"],
-                             w.k, x_bf16=w.x_dtype == "bf16", tokens=toks, expert_ids=inp["expert_ids"])
-            done += n
+                             w.k, x_bf16=w.x_dtype == "bf16", tokens=inp["tokens"], expert_ids=inp["expert_ids"])
+            done += len(inp["tokens"])
         el = time.perf_counter() - t0
         if el >= budget_s:
             return done / el, done, el, threads
 
 
-def host_layer_for_oracle(w, layer, dev_w, x_host, idx_dev):
-    """Host copies of what the oracle needs for one layer: x, router, the used experts, shared."""
-    def bits(t):
-        return t.contiguous().view(__import__("torch").int16).cpu().numpy().view(np.uint16)
+def host_layer_for_oracle(w, layer, dev_w, x_host, n_tokens=8, seed=0):
+    """Host copies of what the oracle needs for a sample of one layer's tokens:
+    x, the router, the experts the oracle routes those tokens to, the shared expert."""
+    import torch
 
-    used = np.unique(idx_dev)
-    return dict(x=(x_host.numpy() if w.x_dtype == "f32" else bits(x_host)),
-                router_w=dev_w["router_w"].cpu().numpy(),
-                router_b=None if dev_w["router_b"] is None else dev_w["router_b"].cpu().numpy(),
-                gate_up=bits(dev_w["gate_up"][used]), down=bits(dev_w["down"][used]),
-                shared=None if dev_w["shared"] is None else bits(dev_w["shared"]), expert_ids=used)
+    import oracle
+
+    def bits(t):
+        return t.contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+
+    x = x_host.numpy() if w.x_dtype == "f32" else bits(x_host)
+    wr = dev_w["router_w"].cpu().numpy()
+    rb = None if dev_w["router_b"] is None else dev_w["router_b"].cpu().numpy()
+    rng = np.random.default_rng(seed + layer)
+    toks = np.sort(rng.choice(w.T, min(w.T, n_tokens), replace=False))
+    logits = oracle.router_logits(oracle.as_f64(x, w.x_dtype == "bf16")[toks], wr.astype(np.float64), rb)
+    used = np.unique(oracle.route(logits, w.k)[0])
+    return dict(x=x, router_w=wr, router_b=rb, gate_up=bits(dev_w["gate_up"][torch.from_numpy(used).to(
+        dev_w["gate_up"].device)]), down=bits(dev_w["down"][torch.from_numpy(used).to(dev_w["down"].device)]),
+        shared=None if dev_w["shared"] is None else bits(dev_w["shared"]), expert_ids=used, tokens=toks)
+
+
+# ------------------------------------------------------------------ multi-rank bookkeeping
+def aggregate(ms, ms_e2e, steps, tokens_per_step, world, dev):
+    """Whole-job throughput: every rank ran `steps` steps of `tokens_per_step`
+    tokens; the job took as long as its slowest rank (all-reduce MAX).
+
+    Returns (tokens/s over all ranks, ms per step of the slowest rank, e2e tokens/s)."""
+    if world > 1:
+        import torch
+
+        t = torch.tensor([ms, ms_e2e], dtype=torch.float64, device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms, ms_e2e = t.tolist()
+    ms_step = ms / steps
+    value = tokens_per_step * world / (ms_step / 1e3)
+    e2e_value = tokens_per_step * world / (ms_e2e / steps / 1e3)
+    return value, ms_step, e2e_value
+
+
+def replica_layer(layer: int, rank: int) -> int:
+    """Seed index of a rank's inputs: every replica draws its own tokens."""
+    return layer + 1000 * rank
 
 
 # ------------------------------------------------------------------ main arm
@@ -221,7 +256,7 @@ def run_ours(args, rank, world, dev):
     stream = torch.cuda.Stream(device=dev)
 
     weights = [device_weights(w, L, dev) for L in range(layers)]
-    xh = [host_x(w, L).pin_memory() for L in range(layers)]
+    xh = [host_x(w, replica_layer(L, rank)).pin_memory() for L in range(layers)]
     xd = [t.to(dev) for t in xh]
     yd = [torch.empty_like(t) for t in xd]
     yh = [torch.empty_like(t).pin_memory() for t in xh]
@@ -255,8 +290,9 @@ def run_ours(args, rank, world, dev):
         for _ in range(max(args.warmup, 0)):
             step()
     stream.synchronize()
-    if ctx.status() != moe.MOE_OK:
-        raise RuntimeError("device status after warm-up: " + moe.moe_strerror(ctx.status()))
+    st = ctx.status()
+    if st != moe.MOE_OK:
+        raise RuntimeError("device status after warm-up: " + moe.moe_strerror(st))
 
     def make_events(n):
         evs = []
@@ -314,26 +350,21 @@ def run_ours(args, rank, world, dev):
     ms, kern_ms, launches = timed(args.steps, e2e=False)
     clk = clocks.stop()
     ms_e2e, _, _ = timed(args.steps, e2e=True)
-    if ctx.status() != moe.MOE_OK:
-        raise RuntimeError("device status after timing: " + moe.moe_strerror(ctx.status()))
+    st = ctx.status()
+    if st != moe.MOE_OK:
+        raise RuntimeError("device status after timing: " + moe.moe_strerror(st))
 
-    if world > 1:
-        t = torch.tensor([ms, ms_e2e], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms, ms_e2e = t.tolist()
-    ms_step = ms / args.steps
     tokens_step = w.T * layers
-    value = tokens_step * world / (ms_step / 1e3)
-    e2e_value = tokens_step * world / (ms_e2e / args.steps / 1e3)
+    value, ms_step, e2e_value = aggregate(ms, ms_e2e, args.steps, tokens_step, world, dev)
 
     # roofline of the dominant kernel: algorithmic bytes (or flops) per launch / mean launch time
     kern_avg_ms = statistics.mean(kern_ms) if kern_ms else None
     if eff_path == moe.MOE_PATH_GEMV:
-        per_launch = statistics.mean(c["gate_up_bytes"] for c in costs)
+        per_launch = statistics.mean(c["layer_bytes"] for c in costs)
         achieved = per_launch / (kern_avg_ms / 1e3) / 1e9
         roof = dict(bound="hbm", achieved=round(achieved, 1), peak=peaks["hbm_gbs"], unit="GB/s",
                     frac=round(achieved / peaks["hbm_gbs"], 4), traffic=None,
-                    kernel="gemv_gate_up_kernel", algorithmic_bytes_per_launch=int(per_launch),
+                    kernel="decode_fused_kernel (whole layer)", algorithmic_bytes_per_launch=int(per_launch),
                     avg_launch_us=round(kern_avg_ms * 1e3, 2), peak_source=peaks["source"])
     else:
         per_launch_b = statistics.mean(c["gate_up_bytes"] for c in costs)
@@ -363,14 +394,10 @@ def run_ours(args, rank, world, dev):
     if rank == 0:
         cpu = None
         if not args.no_cpu_baseline and world == 1:
-            hosts = []
-            for L in range(layers):
-                p = weights[L]
-                r = ctx.route(xd[L], p["router_w"], p["router_b"], stream=stream)
-                hosts.append(host_layer_for_oracle(w, L, p, xh[L], r["idx"].cpu().numpy()))
+            hosts = [host_layer_for_oracle(w, L, weights[L], xh[L]) for L in range(layers)]
             v, n, el, thr = oracle_sample(w, args.cpu_seconds, hosts)
             cpu = dict(value=round(v, 3), unit=UNIT, cores=thr, kind="oracle",
-                       sample=f"{n} token-layers (<=8 random tokens per layer, all {layers} layers, repeated) "
+                       sample=f"{n} token-layers (8 random tokens per layer, all {layers} layers, repeated) "
                               f"in {el:.1f} s; fp64 numpy, BLAS threads = {thr}")
         out = dict(metric=METRIC, value=round(value, 1), unit=UNIT, n_gpus=world, steps=args.steps,
                    warmup=args.warmup, ms_per_step=round(ms_step, 5), higher_is_better=True, scaling="weak",
@@ -391,19 +418,18 @@ def run_ours(args, rank, world, dev):
 def run_reference(args):
     """The fp64 oracle on the host cores, on a bounded sample of the same workload."""
     w = mw.WORKLOADS[args.workload]
-    import oracle  # noqa: F401  (test infrastructure; this leg times it as the CPU baseline)
+    import oracle as orc
 
     hosts = []
     for L in range(w.layers):
         wr, b = mw.draw_router(w, L)
         x = mw.draw_x(w, L)
-        import oracle as orc
-        logits = orc.router_logits(orc.as_f64(x, w.x_dtype == "bf16"), wr.astype(np.float64), b)
-        idx, _, _ = orc.route(logits, w.k)
-        used = np.unique(idx)
+        toks = np.sort(np.random.default_rng(L).choice(w.T, min(w.T, 8), replace=False))
+        logits = orc.router_logits(orc.as_f64(x, w.x_dtype == "bf16")[toks], wr.astype(np.float64), b)
+        used = np.unique(orc.route(logits, w.k)[0])
         gu, dn = mw.draw_experts(w, L, used)
         hosts.append(dict(x=x, router_w=wr, router_b=b, gate_up=gu, down=dn, shared=mw.draw_shared(w, L),
-                          expert_ids=used))
+                          expert_ids=used, tokens=toks))
     for _ in range(max(args.warmup, 0)):
         oracle_sample(w, 0.0, hosts)
     per = []

@@ -20,7 +20,7 @@ MOE_F32, MOE_BF16 = 0, 1
 MOE_PATH_AUTO, MOE_PATH_GEMV, MOE_PATH_GEMM = 0, 1, 2
 MOE_ROUTER_AUTO, MOE_ROUTER_SIMT, MOE_ROUTER_TENSOR = 0, 1, 2
 (MOE_K_ROUTER, MOE_K_SELECT, MOE_K_GROUP, MOE_K_GEMV_GATE_UP, MOE_K_GEMV_DOWN, MOE_K_GEMM_GATE_UP, MOE_K_GEMM_DOWN,
- MOE_K_COMBINE) = range(8)
+ MOE_K_COMBINE, MOE_K_DECODE_FUSED, MOE_K_PERMUTE) = range(10)
 
 HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "moe.h")
 
@@ -53,6 +53,8 @@ def lib() -> ctypes.CDLL:
         L.moe_set_path.argtypes = [P, I]
         L.moe_set_router.argtypes = [P, I]
         L.moe_set_spin_limit.argtypes = [P, ctypes.c_longlong]
+        L.moe_inject_stall.argtypes = [P, I]
+        L.moe_inject_stall.restype = I
         L.moe_time_kernel.argtypes = [P, I, P, P]
         L.moe_time_kernel.restype = I
         L.moe_launch_count.argtypes = [P]
@@ -129,6 +131,10 @@ def moe_set_router(ctx, router: int) -> None:
 
 def moe_set_spin_limit(ctx, limit_ns: int) -> None:
     _check(lib().moe_set_spin_limit(ctx, limit_ns), "moe_set_spin_limit")
+
+
+def moe_inject_stall(ctx, on: bool) -> None:
+    _check(lib().moe_inject_stall(ctx, int(on)), "moe_inject_stall")
 
 
 def moe_time_kernel(ctx, kernel_id: int, ev_start, ev_stop) -> None:

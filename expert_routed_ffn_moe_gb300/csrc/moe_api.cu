@@ -22,7 +22,9 @@ struct moe_ctx {
   int path = MOE_PATH_AUTO;
   int router = MOE_ROUTER_AUTO;
   long long spin_ns = 0;
+  int stall = 0;            // test hook (moe_inject_stall)
   int gemv_max_t = 0;       // largest T the GEMV kernels accept for this shape (0: none)
+  int decode_max_t = 0;     // largest T the fused decode kernel accepts (0: none)
   void* block = nullptr;    // the single device allocation holding all scratch
   Scratch sc{};
   EncodeTiledFn encode = nullptr;
@@ -97,6 +99,7 @@ DevCtl devctl(const moe_ctx* ctx) {
   DevCtl d;
   d.status = ctx->sc.status;
   d.spin_limit = ctx->spin_ns;
+  d.stall = ctx->stall;
   return d;
 }
 
@@ -195,7 +198,8 @@ int moe_init(const moe_config* cfg, moe_ctx** out) {
   if (cudaGetDeviceProperties(&prop, dev) != cudaSuccess) return MOE_ERR_CUDA;
   if (!(prop.major == 10 && prop.minor == 3)) return MOE_ERR_UNSUPPORTED;
 
-  if (prepare_gemm_kernels() != cudaSuccess || prepare_gemv_kernels(kGemvSmemLimit) != cudaSuccess) {
+  if (prepare_gemm_kernels() != cudaSuccess || prepare_gemv_kernels(kGemvSmemLimit) != cudaSuccess ||
+      prepare_decode_kernels(kGemvSmemLimit) != cudaSuccess) {
     cudaGetLastError();
     return MOE_ERR_CUDA;
   }
@@ -207,6 +211,17 @@ int moe_init(const moe_config* cfg, moe_ctx** out) {
   ctx->num_sms = prop.multiProcessorCount;
   ctx->spin_ns = kDefaultSpinNs;
   ctx->gemv_max_t = gemv_limit(ctx->cfg);
+  for (int t = 1; t <= 16 && t <= c.max_tokens; ++t) {
+    Shapes s1;
+    s1.T = t;
+    s1.d = c.d;
+    s1.E = c.n_experts;
+    s1.I = c.inter;
+    s1.k = c.top_k;
+    s1.has_shared = c.has_shared;
+    s1.x_bf16 = c.x_dtype == MOE_BF16;
+    if (decode_supported(s1, kGemvSmemLimit) && decode_blocks_per_sm(s1) >= 1) ctx->decode_max_t = t;
+  }
 
   void* fn = nullptr;
   cudaDriverEntryPointQueryResult q;
@@ -222,7 +237,7 @@ int moe_init(const moe_config* cfg, moe_ctx** out) {
   const size_t T = c.max_tokens, k = c.top_k, E = c.n_experts, d = c.d, I = c.inter;
   const size_t nchunk = (T + kChunk - 1) / kChunk;
   const size_t rows = T * k + T;
-  const size_t tg = ctx->gemv_max_t;
+  const size_t tg = ctx->gemv_max_t > ctx->decode_max_t ? ctx->gemv_max_t : ctx->decode_max_t;
   const int max_mtiles = (int)(T * k / kBM + E + T / kBM + 2);
   size_t off = 0;
   auto take = [&](size_t bytes) {
@@ -243,12 +258,13 @@ int moe_init(const moe_config* cfg, moe_ctx** out) {
   const size_t o_meta = take(4 * 4);
   const size_t o_active = take((E + 1) * 4);
   const size_t o_tickets = take(4 * 4);
-  const size_t o_xbf = take(c.x_dtype == MOE_F32 ? T * d * 2 : 16);
+  const size_t o_xperm = take(rows * d * 2);
   const size_t o_wrs = take(3 * E * d * 2);
   const size_t o_h = take(rows * I * 2);
   const size_t o_hg = take(tg ? (tg * k + tg) * I * 4 : 16);
   const size_t o_out = take(rows * d * 2);
   const size_t o_status = take(16);
+  const size_t o_gridbar = take(16);
   if (cudaMalloc(&ctx->block, off) != cudaSuccess) {
     cudaGetLastError();
     delete ctx;
@@ -274,12 +290,13 @@ int moe_init(const moe_config* cfg, moe_ctx** out) {
   sc.meta = reinterpret_cast<int*>(b + o_meta);
   sc.active = reinterpret_cast<int*>(b + o_active);
   sc.tickets = reinterpret_cast<unsigned*>(b + o_tickets);
-  sc.x_bf16 = reinterpret_cast<uint16_t*>(b + o_xbf);
+  sc.x_perm = reinterpret_cast<uint16_t*>(b + o_xperm);
   sc.wr_split = reinterpret_cast<uint16_t*>(b + o_wrs);
   sc.h = reinterpret_cast<uint16_t*>(b + o_h);
   sc.h_gemv = reinterpret_cast<float*>(b + o_hg);
   sc.out = reinterpret_cast<uint16_t*>(b + o_out);
   sc.status = reinterpret_cast<unsigned*>(b + o_status);
+  sc.gridbar = reinterpret_cast<unsigned*>(b + o_gridbar);
   sc.max_mtiles = max_mtiles;
   *out = ctx;
   return MOE_OK;
@@ -303,8 +320,14 @@ int moe_set_spin_limit(moe_ctx* ctx, long long limit) {
   return MOE_OK;
 }
 
+int moe_inject_stall(moe_ctx* ctx, int on) {
+  if (!ctx || (on != 0 && on != 1)) return MOE_ERR_ARG;
+  ctx->stall = on;
+  return MOE_OK;
+}
+
 int moe_time_kernel(moe_ctx* ctx, int kernel_id, void* ev_start, void* ev_stop) {
-  if (!ctx || kernel_id < MOE_K_ROUTER || kernel_id > MOE_K_COMBINE || !ev_start || !ev_stop) return MOE_ERR_ARG;
+  if (!ctx || kernel_id < MOE_K_ROUTER || kernel_id > MOE_K_PERMUTE || !ev_start || !ev_stop) return MOE_ERR_ARG;
   ctx->timed_kernel = kernel_id;
   ctx->ev_start = static_cast<cudaEvent_t>(ev_start);
   ctx->ev_stop = static_cast<cudaEvent_t>(ev_stop);
@@ -328,7 +351,7 @@ int moe_route(moe_ctx* ctx, const void* x, int T, const float* router_w, const f
   memset(&maps, 0, sizeof(maps));
   if (tensor) {
     if ((rc = make_map(ctx, &maps.x_tile, x, s.d, s.T, 64, 128)) != MOE_OK) return rc;
-    if ((rc = make_map(ctx, &maps.wr_split, ctx->sc.wr_split, s.d, 3 * s.E, 64, 128)) != MOE_OK) return rc;
+    if ((rc = make_map(ctx, &maps.wr_split, ctx->sc.wr_split, s.d, 3 * s.E, 64, 256)) != MOE_OK) return rc;
   }
   if ((rc = run_route(ctx, s, x, router_w, router_b, tensor, &maps, st)) != MOE_OK) return rc;
   return cuda_fail(launch_export_route(s, ctx->sc, idx, w, counts, offsets, perm, st));
@@ -349,13 +372,22 @@ int moe_forward(moe_ctx* ctx, const void* x, int T, const float* router_w, const
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const Shapes s = shapes(ctx, T, top_k);
   int path = ctx->path;
-  if (path == MOE_PATH_AUTO) path = (T <= kGemvMaxT && T <= ctx->gemv_max_t) ? MOE_PATH_GEMV : MOE_PATH_GEMM;
-  if (path == MOE_PATH_GEMV && T > ctx->gemv_max_t) return MOE_ERR_UNSUPPORTED;
+  const int small_max = ctx->gemv_max_t > ctx->decode_max_t ? ctx->gemv_max_t : ctx->decode_max_t;
+  if (path == MOE_PATH_AUTO) path = (T <= kGemvMaxT && T <= small_max) ? MOE_PATH_GEMV : MOE_PATH_GEMM;
+  if (path == MOE_PATH_GEMV && T > small_max) return MOE_ERR_UNSUPPORTED;
   const DevCtl ctl = devctl(ctx);
   const uint16_t* gu = static_cast<const uint16_t*>(experts_gate_up);
   const uint16_t* dn = static_cast<const uint16_t*>(experts_down);
   const uint16_t* sw = static_cast<const uint16_t*>(shared_w);
 
+  if (path == MOE_PATH_GEMV && T <= ctx->decode_max_t) {
+    // the whole layer in one cooperative launch
+    const cudaError_t err = launch(ctx, MOE_K_DECODE_FUSED, st, [&] {
+      return launch_decode_fused(s, x, router_w, router_b, gu, dn, sw, y, ctx->sc, ctl, ctx->sc.gridbar,
+                                 ctx->num_sms, st);
+    });
+    return cuda_fail(err);
+  }
   if (path == MOE_PATH_GEMV) {
     if ((rc = run_route(ctx, s, x, router_w, router_b, false, nullptr, st)) != MOE_OK) return rc;
     const Scratch& sc = ctx->sc;
@@ -369,22 +401,15 @@ int moe_forward(moe_ctx* ctx, const void* x, int T, const float* router_w, const
 
   // grouped-GEMM path
   const bool tensor = use_tensor_router(ctx, s);
-  const void* xb = x;
-  if (!s.x_bf16) {
-    cudaError_t err =
-        launch(ctx, -3, st, [&] { return launch_x_to_bf16(s, static_cast<const float*>(x), ctx->sc, st); });
-    if (err != cudaSuccess) return MOE_ERR_CUDA;
-    xb = ctx->sc.x_bf16;
-  }
   GemmMaps maps;
   memset(&maps, 0, sizeof(maps));
   const uint64_t rows = (uint64_t)s.T * s.k + (s.has_shared ? s.T : 0);
-  if ((rc = make_map(ctx, &maps.x_rows, xb, s.d, s.T, 64, 1)) != MOE_OK) return rc;
-  if ((rc = make_map(ctx, &maps.x_tile, xb, s.d, s.T, 64, 128)) != MOE_OK) return rc;
+  if (s.x_bf16 && (rc = make_map(ctx, &maps.x_tile, x, s.d, s.T, 64, 128)) != MOE_OK) return rc;
+  if ((rc = make_map(ctx, &maps.x_perm, ctx->sc.x_perm, s.d, rows, 64, 128)) != MOE_OK) return rc;
   if ((rc = make_map(ctx, &maps.gate_up, gu, s.d, (uint64_t)s.E * 2 * s.I, 64, 128)) != MOE_OK) return rc;
   if ((rc = make_map(ctx, &maps.h, ctx->sc.h, s.I, rows, 64, 128)) != MOE_OK) return rc;
   if ((rc = make_map(ctx, &maps.down, dn, s.I, (uint64_t)s.E * s.d, 64, 256)) != MOE_OK) return rc;
-  if ((rc = make_map(ctx, &maps.wr_split, ctx->sc.wr_split, s.d, 3 * s.E, 64, 128)) != MOE_OK) return rc;
+  if ((rc = make_map(ctx, &maps.wr_split, ctx->sc.wr_split, s.d, 3 * s.E, 64, 256)) != MOE_OK) return rc;
   // without a shared expert these maps are never read; point them at routed weights
   const uint16_t* sgu = sw ? sw : gu;
   const uint16_t* sdn = sw ? sw + (size_t)2 * s.I * s.d : dn;
@@ -394,8 +419,9 @@ int moe_forward(moe_ctx* ctx, const void* x, int T, const float* router_w, const
   if ((rc = run_route(ctx, s, x, router_w, router_b, tensor, &maps, st)) != MOE_OK) return rc;
   const Scratch& sc = ctx->sc;
   const int sms = ctx->num_sms;
-  cudaError_t err =
-      launch(ctx, MOE_K_GEMM_GATE_UP, st, [&] { return launch_gemm_gate_up(s, maps, sc, ctl, sms, st); });
+  cudaError_t err = launch(ctx, MOE_K_PERMUTE, st, [&] { return launch_permute_rows(s, x, sc, ctl, st); });
+  if (err == cudaSuccess)
+    err = launch(ctx, MOE_K_GEMM_GATE_UP, st, [&] { return launch_gemm_gate_up(s, maps, sc, ctl, sms, st); });
   if (err == cudaSuccess)
     err = launch(ctx, MOE_K_GEMM_DOWN, st, [&] { return launch_gemm_down(s, maps, sc, ctl, sms, st); });
   if (err == cudaSuccess) err = launch(ctx, MOE_K_COMBINE, st, [&] { return launch_combine(s, y, sc, st); });
@@ -408,6 +434,8 @@ int moe_status(moe_ctx* ctx) {
   unsigned v = 0;
   if (cudaMemcpy(&v, ctx->sc.status, 4, cudaMemcpyDeviceToHost) != cudaSuccess) return MOE_ERR_CUDA;
   if (v && cudaMemset(ctx->sc.status, 0, 4) != cudaSuccess) return MOE_ERR_CUDA;
+  // a kernel that gave up may have left the grid-barrier counters mid-way
+  if ((v & kStatusTimeout) && cudaMemset(ctx->sc.gridbar, 0, 8) != cudaSuccess) return MOE_ERR_CUDA;
   if (v & kStatusTimeout) return MOE_ERR_TIMEOUT;
   if (v & kStatusBounds) return MOE_ERR_BOUNDS;
   return MOE_OK;

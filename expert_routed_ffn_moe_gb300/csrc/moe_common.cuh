@@ -23,6 +23,7 @@ enum : unsigned { kStatusTimeout = 1u, kStatusBounds = 2u };
 struct DevCtl {
   unsigned* status;        // device status word
   long long spin_limit;    // nanoseconds a bounded wait polls before giving up
+  int stall;               // test hook: 1 = wait once on a barrier nothing signals (see moe_inject_stall)
 };
 
 MOE_DEV void raise_status(const DevCtl& c, unsigned bit) { atomicOr(c.status, bit); }
@@ -68,19 +69,22 @@ MOE_DEV bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
-MOE_DEV uint64_t global_ns() {
-  uint64_t t;
-  asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
-  return t;
-}
+// Deadline of a bounded wait in SM clock cycles.  The limit is given in
+// nanoseconds; 2 cycles per ns matches the 2.07 GHz top clock, so at lower
+// clocks a wait may last somewhat longer than the limit, never shorter.
+MOE_DEV long long wait_cycles(const DevCtl& c) { return c.spin_limit * 2; }
+
 // Bounded wait: false (and the timeout bit raised) once the barrier has not
-// completed within c.spin_limit nanoseconds of GPU global time.
+// completed within the limit.  The cycle counter is read only every 256 polls
+// so that checking the deadline never delays noticing a completed phase.
 MOE_DEV bool mbar_wait(uint64_t* bar, uint32_t parity, const DevCtl& c) {
   if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = global_ns();
+  const long long t0 = clock64(), lim = wait_cycles(c);
   while (true) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((long long)(global_ns() - t0) > c.spin_limit) break;
+#pragma unroll 1
+    for (int i = 0; i < 256; ++i)
+      if (mbar_try_wait(bar, parity)) return true;
+    if (clock64() - t0 > lim) break;
   }
   raise_status(c, kStatusTimeout);
   return false;
@@ -97,20 +101,14 @@ MOE_DEV void tma_load_2d(void* dst, const CUtensorMap* m, int c0, int c1, uint64
       "l"(reinterpret_cast<uint64_t>(m)), "r"(c0), "r"(c1), "r"(smem_u32(bar)), "l"(policy)
       : "memory");
 }
-// Four rows (r0..r3) of a 2D tensor whose box is one row high, columns c0.., into
-// four consecutive box-sized slots at dst.
-MOE_DEV void tma_gather4(void* dst, const CUtensorMap* m, int c0, int r0, int r1, int r2, int r3,
-                         uint64_t* bar, uint64_t policy) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes.L2::cache_hint"
-      " [%0], [%1, {%2, %3, %4, %5, %6}], [%7], %8;" ::"r"(smem_u32(dst)),
-      "l"(reinterpret_cast<uint64_t>(m)), "r"(c0), "r"(r0), "r"(r1), "r"(r2), "r"(r3),
-      "r"(smem_u32(bar)), "l"(policy)
-      : "memory");
-}
 MOE_DEV uint64_t policy_evict_first() {
   uint64_t p;
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+MOE_DEV uint64_t policy_evict_normal() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(p));
   return p;
 }
 MOE_DEV uint64_t policy_evict_last() {

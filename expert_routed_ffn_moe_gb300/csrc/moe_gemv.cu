@@ -64,7 +64,11 @@ __global__ void __launch_bounds__(kGemvWarps * 32) gemv_gate_up_kernel(Shapes s,
   const int nch = s.d >> 8;
   const int n_active = sc.meta[1];
   const int units = n_active * s.I;
-  for (int u = blockIdx.x * kGemvWarps + warp; u < units; u += gridDim.x * kGemvWarps) {
+  // units are dealt to blocks first (u = block + j * grid), so every SM streams
+  // the same number of weight bytes to within one unit
+  for (int j = warp;; j += kGemvWarps) {
+    const int u = blockIdx.x + j * gridDim.x;
+    if (u >= units) break;
     const int a = u / s.I, i = u - a * s.I;
     const int e = sc.active[a];
     if (e < 0 || e > s.E || (e == s.E && !s.has_shared)) {
@@ -139,7 +143,9 @@ __global__ void __launch_bounds__(kGemvWarps * 32) gemv_down_kernel(Shapes s, co
   __syncthreads();
   const int nci = s.I >> 8;
   const int n_active = sc.meta[1];
-  for (int r = blockIdx.x * kGemvWarps + warp; r < s.d; r += gridDim.x * kGemvWarps) {
+  for (int j = warp;; j += kGemvWarps) {
+    const int r = blockIdx.x + j * gridDim.x;
+    if (r >= s.d) break;
     float acc = 0.f;  // lane t accumulates token t
     constexpr int kBatch = (16 / MAXCI) > 0 ? (16 / MAXCI) : 1;  // experts whose rows are in flight together
     for (int a0 = 0; a0 < n_active; a0 += kBatch) {

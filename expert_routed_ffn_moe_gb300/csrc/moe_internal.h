@@ -38,12 +38,13 @@ struct Scratch {
   int* meta;              // [0] = number of m-tiles, [1] = number of active experts
   int* active;            // [E + 1]: experts with count > 0, ascending, then the shared expert
   unsigned* tickets;      // last-block counters (self-resetting)
-  uint16_t* x_bf16;       // [T, d] bf16 copy of an fp32 x (GEMM path)
+  uint16_t* x_perm;       // [T*k + T, d] bf16 token rows in grouped order (GEMM path)
   uint16_t* wr_split;     // [3E, d] router weights as bf16 hi + mid + lo terms
   uint16_t* h;            // [T*k + T, I] bf16 SwiGLU activations, grouped rows (GEMM path)
   float* h_gemv;          // [Tg*k + Tg, I] fp32 SwiGLU activations (GEMV path)
   uint16_t* out;          // [T*k + T, d] bf16 expert outputs, grouped rows (GEMM path)
   unsigned* status;       // device status word
+  unsigned* gridbar;      // [2] arrival / departure counters of the fused decode kernel's grid barriers
   int max_mtiles;
 };
 
@@ -74,14 +75,14 @@ cudaError_t launch_gemv_down(const Shapes& s, const uint16_t* down, const uint16
 
 // moe_gemm.cu
 struct GemmMaps {
-  CUtensorMap x_rows;       // x (bf16) [T, d], box 64 x 1 (row gather)
   CUtensorMap x_tile;       // x (bf16) [T, d], box 64 x 128
-  CUtensorMap gate_up;      // experts [E*2I, d], box 64 x 128
+  CUtensorMap x_perm;       // grouped token rows [T*k + T, d], box 64 x 128
+  CUtensorMap gate_up;      // experts [E*2I, d], box 64 x 128 (gate half and up half of one B tile)
   CUtensorMap shared_gu;    // shared gate_up [2I, d], box 64 x 128
   CUtensorMap h;            // h [T*k + T, I], box 64 x 128
   CUtensorMap down;         // experts [E*d, I], box 64 x 256
   CUtensorMap shared_down;  // shared down [d, I], box 64 x 256
-  CUtensorMap wr_split;     // router weights hi/mid/lo [3E, d], box 64 x 128
+  CUtensorMap wr_split;     // router weights hi/mid/lo [3E, d], box 64 x 256
 };
 cudaError_t prepare_gemm_kernels();
 cudaError_t launch_gemm_gate_up(const Shapes& s, const GemmMaps& m, const Scratch& sc, const DevCtl& ctl,
@@ -91,8 +92,18 @@ cudaError_t launch_gemm_down(const Shapes& s, const GemmMaps& m, const Scratch& 
 cudaError_t launch_gemm_router(const Shapes& s, const GemmMaps& m, const Scratch& sc, const DevCtl& ctl,
                                int num_sms, cudaStream_t st);
 
+// moe_decode.cu
+size_t decode_smem_bytes(const Shapes& s);
+bool decode_supported(const Shapes& s, int max_smem);
+int decode_blocks_per_sm(const Shapes& s);
+cudaError_t prepare_decode_kernels(int max_smem);
+cudaError_t launch_decode_fused(const Shapes& s, const void* x, const float* wr, const float* rb,
+                                const uint16_t* gate_up, const uint16_t* down, const uint16_t* shared_w, void* y,
+                                const Scratch& sc, const DevCtl& ctl, unsigned* bar, int num_sms, cudaStream_t st);
+
 // moe_combine.cu
-cudaError_t launch_x_to_bf16(const Shapes& s, const float* x, const Scratch& sc, cudaStream_t st);
+cudaError_t launch_permute_rows(const Shapes& s, const void* x, const Scratch& sc, const DevCtl& ctl,
+                                cudaStream_t st);
 cudaError_t launch_combine(const Shapes& s, void* y, const Scratch& sc, cudaStream_t st);
 
 }  // namespace moe

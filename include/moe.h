@@ -62,7 +62,9 @@ extern "C" {
 
 /* execution path for the expert FFNs (moe_set_path) */
 #define MOE_PATH_AUTO 0        /* small T: GEMV over the selected experts; otherwise grouped GEMM */
-#define MOE_PATH_GEMV 1        /* bandwidth-bound GEMV (only for small T, else MOE_ERR_UNSUPPORTED) */
+#define MOE_PATH_GEMV 1        /* bandwidth-bound GEMV over the selected experts (small T only, else
+                                  MOE_ERR_UNSUPPORTED); for T <= 16 when shapes allow, the whole layer
+                                  runs as one cooperative kernel with two grid barriers */
 #define MOE_PATH_GEMM 2        /* tcgen05/TMEM grouped GEMM */
 
 /* router logit kernel (moe_set_router) */
@@ -132,8 +134,9 @@ int moe_set_router(moe_ctx* ctx, int router);
  * reported an error. */
 int moe_status(moe_ctx* ctx);
 
-/* Test hook for the bounded waits: how long (nanoseconds of GPU global time)
- * a kernel polls a barrier before giving up with MOE_ERR_TIMEOUT.  0 restores
+/* Bounded waits: how long (nanoseconds, measured in SM clock cycles at 2 per
+ * ns) a kernel polls a barrier before giving up with MOE_ERR_TIMEOUT.  A wait
+ * always polls at least 256 times before it looks at the clock.  0 restores
  * the default (1 s).  MOE_ERR_ARG if negative. */
 int moe_set_spin_limit(moe_ctx* ctx, long long limit);
 
@@ -146,6 +149,8 @@ int moe_set_spin_limit(moe_ctx* ctx, long long limit);
 #define MOE_K_GEMM_GATE_UP 5   /* grouped GEMM: gate/up projections + SwiGLU */
 #define MOE_K_GEMM_DOWN 6      /* grouped GEMM: down projection */
 #define MOE_K_COMBINE 7        /* grouped-GEMM path: weighted combine + shared */
+#define MOE_K_DECODE_FUSED 8   /* small-T path: the whole layer in one cooperative kernel */
+#define MOE_K_PERMUTE 9        /* grouped-GEMM path: token rows copied into expert-grouped order */
 
 /* Profiling hook: the next moe_forward/moe_route call on `ctx` records the
  * CUDA events `ev_start` / `ev_stop` (cudaEvent_t, created by the caller with
@@ -157,6 +162,15 @@ int moe_time_kernel(moe_ctx* ctx, int kernel_id, void* ev_start, void* ev_stop);
 
 /* Number of kernels this context has launched (or captured) so far. */
 long long moe_launch_count(moe_ctx* ctx);
+
+/* Test hook for failure detection without a GPU fault: with on = 1, later
+ * calls make the grouped GEMM's MMA thread, and every block of the fused
+ * decode kernel at its first grid barrier, wait once for an event that never
+ * happens.  The bounded wait runs out after the spin limit, the kernel records
+ * MOE_ERR_TIMEOUT, drains its in-flight copies, frees its tensor memory and
+ * returns; moe_status then reports the timeout.  on = 0 turns it off.
+ * MOE_ERR_ARG on other values. */
+int moe_inject_stall(moe_ctx* ctx, int on);
 
 /* Static description of a return code. */
 const char* moe_strerror(int code);

@@ -177,17 +177,20 @@ def test_argument_errors():
 
 
 def test_bounded_wait_reports_timeout_and_context_recovers():
-    # A 1 ns limit makes the first barrier wait that is not already complete
-    # give up: the grouped GEMM must return with MOE_ERR_TIMEOUT latched (no
-    # trap, no hang), and the same context must then run correctly again.
+    # The injected stall makes the grouped GEMM's MMA thread wait on a barrier
+    # nothing signals; with a 1 ms limit the wait runs out, the kernel must
+    # return with MOE_ERR_TIMEOUT latched (no trap, no hang), and the same
+    # context must then run correctly again.
     w = custom("timeout", T=256)
     inp = layer_inputs(w)
     layer = make_layer(w, path=moe.MOE_PATH_GEMM)
     d = device_inputs(w, inp)
     args = (d["router_w"], d["router_b"], d["gate_up"], d["down"], d["shared"])
-    moe.moe_set_spin_limit(layer.ctx, 1)
+    moe.moe_set_spin_limit(layer.ctx, 1_000_000)
+    moe.moe_inject_stall(layer.ctx, True)
     layer.forward(d["x"], *args)
     assert layer.status() == moe.MOE_ERR_TIMEOUT
+    moe.moe_inject_stall(layer.ctx, False)
     moe.moe_set_spin_limit(layer.ctx, 0)
     y = layer.forward(d["x"], *args)
     torch.cuda.synchronize()
@@ -195,3 +198,34 @@ def test_bounded_wait_reports_timeout_and_context_recovers():
     layer.close()
     toks = sample_tokens(w.T, 32)
     check_y(y_host(y)[toks], oracle_y(w, inp, toks), "after timeout")
+
+
+def test_modular_gemv_path_beyond_fused_limit():
+    # T = 24 with d = 512, I = 256: above the fused decode kernel's 16-token
+    # limit, still inside the GEMV kernels' shared-memory limit
+    full_case(custom("gemv24", T=24), path=moe.MOE_PATH_GEMV)
+
+
+def test_fused_decode_barrier_timeout_and_recovery():
+    # The injected stall makes every block wait at the first grid barrier for
+    # one arrival more than there are blocks; with a 1 ms limit the wait runs
+    # out, the status word reports it, moe_status resets the barrier counters,
+    # and the next call on the same context is correct.
+    w = W["decode"]
+    inp = layer_inputs(w, 2)
+    layer = make_layer(w)
+    d = device_inputs(w, inp)
+    args = (d["router_w"], d["router_b"], d["gate_up"], d["down"], d["shared"])
+    moe.moe_set_spin_limit(layer.ctx, 1_000_000)
+    moe.moe_inject_stall(layer.ctx, True)
+    layer.forward(d["x"], *args)
+    assert layer.status() == moe.MOE_ERR_TIMEOUT
+    moe.moe_inject_stall(layer.ctx, False)
+    moe.moe_set_spin_limit(layer.ctx, 0)
+    y = layer.forward(d["x"], *args)
+    y2 = layer.forward(d["x"], *args)
+    torch.cuda.synchronize()
+    assert layer.status() == moe.MOE_OK
+    layer.close()
+    assert torch.equal(y, y2)
+    check_y(y_host(y), oracle_y(w, inp, [0]), "after barrier timeout")
