@@ -59,6 +59,8 @@ def lib() -> ctypes.CDLL:
         L.moe_time_kernel.restype = I
         L.moe_launch_count.argtypes = [P]
         L.moe_launch_count.restype = ctypes.c_longlong
+        L.moe_decode_noalloc.argtypes = [P, I, I, I, I, I, I, P, P, P, P, P, P, P, P]
+        L.moe_decode_noalloc.restype = I
         L.moe_status.argtypes = [P]
         L.moe_strerror.argtypes = [I]
         L.moe_strerror.restype = ctypes.c_char_p
@@ -174,6 +176,26 @@ def moe_forward(ctx, x, router_w, router_b, experts_gate_up, experts_down, share
         _need_cuda(t, name, dt)
     _check(lib().moe_forward(ctx, _ptr(x), x.shape[0], _ptr(router_w), _ptr(router_b), _ptr(experts_gate_up),
                              _ptr(experts_down), _ptr(shared_w), top_k, _ptr(y), _stream(stream)), "moe_forward")
+
+
+def moe_decode_noalloc(x, router_w, router_b, experts_gate_up, experts_down, shared_w, top_k, y, status=None,
+                       stream=None) -> None:
+    """The small-T layer without a context: for callers that cannot allocate
+    device memory (inside a stream capture, or under a no-allocation policy).
+    Scratch memory is a fixed device array inside the library; see moe.h."""
+    import torch
+
+    for name, t, dt in (("x", x, None), ("router_w", router_w, torch.float32), ("router_b", router_b, torch.float32),
+                        ("experts_gate_up", experts_gate_up, torch.bfloat16),
+                        ("experts_down", experts_down, torch.bfloat16), ("shared_w", shared_w, torch.bfloat16),
+                        ("y", y, x.dtype), ("status", status, torch.int32)):
+        _need_cuda(t, name, dt)
+    T, d = x.shape
+    E, inter = experts_down.shape[0], experts_down.shape[2]
+    x_dtype = MOE_BF16 if x.dtype == torch.bfloat16 else MOE_F32
+    _check(lib().moe_decode_noalloc(_ptr(x), T, x_dtype, d, E, inter, top_k, _ptr(router_w), _ptr(router_b),
+                                    _ptr(experts_gate_up), _ptr(experts_down), _ptr(shared_w), _ptr(y), _ptr(status),
+                                    _stream(stream)), "moe_decode_noalloc")
 
 
 class MoeLayer:

@@ -608,3 +608,127 @@ cudaError_t launch_decode_fused(const Shapes& s, const void* x, const float* wr,
 }
 
 }  // namespace moe
+
+// ---------------------------------------------------------------------------
+// Allocation-free variant of the fused decode layer (moe_decode_noalloc).
+//
+// Some callers cannot call cudaMalloc, so they cannot create a context with
+// moe_init: code that builds its GPU work inside an ongoing CUDA stream capture
+// (allocation is not allowed there), and processes that run under a strict
+// no-allocation policy (real-time serving loops, or hosts whose device memory
+// is owned by another allocator).  For them the same kernel runs on scratch
+// memory that is part of the library image: one file-scope device array, sized
+// for the limits below, that every GPU loading the library holds until exit.
+// The host learns its device address once per device with
+// cudaGetSymbolAddress; the array's name in host code is only a host-side
+// stand-in, never a device address.
+// ---------------------------------------------------------------------------
+#include <mutex>
+
+using namespace moe;
+
+namespace {
+
+constexpr int kNoAllocMaxT = 16;
+constexpr int kNoAllocMaxTopK = 8;
+constexpr int kNoAllocMaxInter = 1024;
+constexpr size_t kNoAllocH = (size_t)kNoAllocMaxT * (kNoAllocMaxTopK + 1) * kNoAllocMaxInter * 4;  // fp32 h rows
+constexpr size_t kNoAllocLogits = (size_t)kNoAllocMaxT * kMaxExperts * 4;
+constexpr size_t kNoAllocPicks = (size_t)kNoAllocMaxT * kNoAllocMaxTopK * 4;
+constexpr size_t kNoAllocOffLogits = kNoAllocH;
+constexpr size_t kNoAllocOffIdx = kNoAllocOffLogits + kNoAllocLogits;
+constexpr size_t kNoAllocOffW = kNoAllocOffIdx + kNoAllocPicks;
+constexpr size_t kNoAllocOffWords = kNoAllocOffW + kNoAllocPicks;  // [0] status, [2..3] barrier counters
+constexpr size_t kNoAllocBytes = kNoAllocOffWords + 256;
+
+struct NoAllocDevice {
+  bool ready = false;
+  unsigned char* base = nullptr;  // device address of the array on this device
+  int sms = 0;
+};
+constexpr int kNoAllocMaxDevices = 64;
+NoAllocDevice g_noalloc_dev[kNoAllocMaxDevices];
+std::mutex g_noalloc_mu;
+
+}  // namespace
+
+// The scratch array (about 600 KB).  Every call shares it and it keeps the
+// last call's contents; the barrier counters, which must start at zero, are
+// cleared at the start of every call.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocBytes];
+
+extern "C" int moe_decode_noalloc(const void* x, int T, int x_dtype, int d, int n_experts, int inter, int top_k,
+                                  const float* router_w, const float* router_b, const void* experts_gate_up,
+                                  const void* experts_down, const void* shared_w, void* y, unsigned* status,
+                                  void* stream) {
+  if (T < 0 || d <= 0 || n_experts <= 0 || inter <= 0 || top_k <= 0) return MOE_ERR_ARG;
+  if (T == 0) return MOE_OK;
+  if (!x || !router_w || !experts_gate_up || !experts_down || !y) return MOE_ERR_ARG;
+  if (x_dtype != MOE_F32 && x_dtype != MOE_BF16) return MOE_ERR_ARG;
+  if (top_k > n_experts) return MOE_ERR_ARG;
+  // the fixed size of the scratch array
+  if (T > kNoAllocMaxT || top_k > kNoAllocMaxTopK || inter > kNoAllocMaxInter || n_experts > kMaxExperts)
+    return MOE_ERR_UNSUPPORTED;
+  const void* ptrs[] = {x, router_w, router_b, experts_gate_up, experts_down, shared_w, y, status};
+  for (const void* p : ptrs)
+    if (p && (reinterpret_cast<uintptr_t>(p) & 15u)) return MOE_ERR_ALIGN;
+  Shapes s{};
+  s.T = T;
+  s.d = d;
+  s.E = n_experts;
+  s.I = inter;
+  s.k = top_k;
+  s.has_shared = shared_w != nullptr;
+  s.x_bf16 = x_dtype == MOE_BF16;
+  const int smem_limit = 200 * 1024;
+  if (!decode_supported(s, smem_limit)) return MOE_ERR_UNSUPPORTED;
+
+  // set-up, once per device, with that device current
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kNoAllocMaxDevices) return MOE_ERR_CUDA;
+  NoAllocDevice nd;
+  {
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    NoAllocDevice& slot = g_noalloc_dev[dev];
+    if (!slot.ready) {
+      cudaDeviceProp prop;
+      if (cudaGetDeviceProperties(&prop, dev) != cudaSuccess) return MOE_ERR_CUDA;
+      if (!(prop.major == 10 && prop.minor == 3)) return MOE_ERR_UNSUPPORTED;
+      void* p = nullptr;
+      if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) {
+        cudaGetLastError();
+        return MOE_ERR_CUDA;
+      }
+      if (prepare_decode_kernels(smem_limit) != cudaSuccess) {
+        cudaGetLastError();
+        return MOE_ERR_CUDA;
+      }
+      slot.base = static_cast<unsigned char*>(p);
+      slot.sms = prop.multiProcessorCount;
+      slot.ready = true;
+    }
+    nd = slot;
+  }
+  if (decode_blocks_per_sm(s) < 1) return MOE_ERR_UNSUPPORTED;
+
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  unsigned* words = reinterpret_cast<unsigned*>(nd.base + kNoAllocOffWords);
+  unsigned* bar = words + 2;
+  if (cudaMemsetAsync(bar, 0, 2 * sizeof(unsigned), st) != cudaSuccess) return MOE_ERR_CUDA;
+  Scratch sc{};
+  sc.h_gemv = reinterpret_cast<float*>(nd.base);
+  sc.logits = reinterpret_cast<float*>(nd.base + kNoAllocOffLogits);
+  sc.idx = reinterpret_cast<int*>(nd.base + kNoAllocOffIdx);
+  sc.w = reinterpret_cast<float*>(nd.base + kNoAllocOffW);
+  sc.status = status ? status : words;
+  sc.gridbar = bar;
+  DevCtl ctl;
+  ctl.status = sc.status;
+  ctl.spin_limit = 1000000000LL;
+  ctl.stall = 0;
+  const cudaError_t err =
+      launch_decode_fused(s, x, router_w, router_b, static_cast<const uint16_t*>(experts_gate_up),
+                          static_cast<const uint16_t*>(experts_down), static_cast<const uint16_t*>(shared_w), y, sc,
+                          ctl, bar, nd.sms, st);
+  return err == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}

@@ -172,6 +172,38 @@ long long moe_launch_count(moe_ctx* ctx);
  * MOE_ERR_ARG on other values. */
 int moe_inject_stall(moe_ctx* ctx, int on);
 
+/* Allocation-free decode layer (no counterpart in the source pages; added for
+ * callers that cannot allocate device memory).  Code that records its GPU work
+ * inside an ongoing CUDA stream capture cannot call cudaMalloc there, and
+ * processes under a strict no-allocation policy (real-time serving loops,
+ * hosts whose device memory belongs to another allocator) must not; neither can
+ * create a context with moe_init.  This entry point runs the same fused decode
+ * kernel as moe_forward's small-T path, but its scratch memory is a fixed
+ * device array inside the library (about 600 KB, held on every GPU that loads
+ * the library until the process exits).  It calls no cudaMalloc, cudaFree or
+ * allocating library routine.
+ *
+ * Inputs and outputs are as for moe_forward, with the shapes passed directly:
+ * x [T, d] (x_dtype), router_w [E, d] fp32, router_b [E] fp32 or NULL,
+ * experts_gate_up [E, 2*inter, d] bf16, experts_down [E, d, inter] bf16,
+ * shared_w (shared gate_up [2*inter, d] then down [d, inter], bf16) or NULL,
+ * y [T, d] (x_dtype).  status: optional device word (NULL = none) into which a
+ * kernel ORs a failure it detects (1 = a bounded wait ran out, 2 = an index was
+ * out of range); it is not cleared by the call.
+ * Limits of the fixed scratch: T <= 16, top_k <= 8, inter <= 1024, E <= 256,
+ * plus the fused kernel's own (d in {512, 1024, 2048}, inter a multiple of 256,
+ * its shared-memory staging); larger shapes return MOE_ERR_UNSUPPORTED before
+ * anything is launched.  The first call on each device looks up the array's
+ * device address (cudaGetSymbolAddress) and sets kernel attributes, with that
+ * device current: make that first call before any stream capture.  Every call
+ * shares the one array, which keeps the previous call's contents (the barrier
+ * counters that must start at zero are cleared by each call on `stream`), so
+ * calls that overlap on the GPU -- on different streams, or from different
+ * threads -- race and must not be issued.  Asynchronous on `stream`. */
+int moe_decode_noalloc(const void* x, int T, int x_dtype, int d, int n_experts, int inter, int top_k,
+                       const float* router_w, const float* router_b, const void* experts_gate_up,
+                       const void* experts_down, const void* shared_w, void* y, unsigned* status, void* stream);
+
 /* Static description of a return code. */
 const char* moe_strerror(int code);
 
