@@ -6,6 +6,7 @@
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
+#include <math.h>
 #include <stdint.h>
 
 #include "moe.h"
@@ -41,6 +42,94 @@ MOE_DEV float warp_sum(float v) {
   return v;
 }
 MOE_DEV float silu(float g) { return g / (1.0f + __expf(-g)); }
+
+// ---------------------------------------------------------------- top-k selection
+// Order-preserving map of an fp32 value to u32 (NaN taken as -inf).
+MOE_DEV uint32_t ordered_key(float v) {
+  if (v != v) v = -INFINITY;
+  const uint32_t u = __float_as_uint(v);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+MOE_DEV float key_value(uint32_t k) { return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k); }
+
+// Compare-exchange of (key, id) pairs into descending key, ascending id.
+MOE_DEV void key_cx(uint32_t& ka, int& ea, uint32_t& kb, int& eb) {
+  const bool swap = (kb > ka) || (kb == ka && eb < ea);
+  const uint32_t k0 = swap ? kb : ka, k1 = swap ? ka : kb;
+  const int e0 = swap ? eb : ea, e1 = swap ? ea : eb;
+  ka = k0;
+  kb = k1;
+  ea = e0;
+  eb = e1;
+}
+
+// Warp-wide top-k of one token's E <= 256 logits, lane l holding the logits of
+// experts l, l+32, ..., l+224 in v[0..7] (-inf past E).  Every lane sorts its
+// 8 (logit, expert) pairs; each of the k rounds takes the warp's largest head
+// with two warp reductions (value, then the lowest expert id among equal
+// values) and the winning lane pops it.  On return lane j < k holds pick j:
+// its expert id, its weight exp(l_j - l_max) / sum over the picks (the softmax
+// over all E renormalised over the picks, common denominator cancelled) and its
+// rank in ascending expert id.  Returns false if some pick was not a number.
+MOE_DEV bool warp_top_k(const float (&v)[8], int E, int k, int lane, int& pick_e, float& pick_w, int& pick_rank) {
+  uint32_t kk[8];
+  int ee[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int e = lane + 32 * i;
+    ee[i] = e < E ? e : 0x7fffffff;
+    kk[i] = e < E ? ordered_key(v[i]) : 0u;
+  }
+  key_cx(kk[0], ee[0], kk[1], ee[1]); key_cx(kk[2], ee[2], kk[3], ee[3]);
+  key_cx(kk[4], ee[4], kk[5], ee[5]); key_cx(kk[6], ee[6], kk[7], ee[7]);
+  key_cx(kk[0], ee[0], kk[2], ee[2]); key_cx(kk[1], ee[1], kk[3], ee[3]);
+  key_cx(kk[4], ee[4], kk[6], ee[6]); key_cx(kk[5], ee[5], kk[7], ee[7]);
+  key_cx(kk[1], ee[1], kk[2], ee[2]); key_cx(kk[5], ee[5], kk[6], ee[6]);
+  key_cx(kk[0], ee[0], kk[4], ee[4]); key_cx(kk[1], ee[1], kk[5], ee[5]);
+  key_cx(kk[2], ee[2], kk[6], ee[6]); key_cx(kk[3], ee[3], kk[7], ee[7]);
+  key_cx(kk[2], ee[2], kk[4], ee[4]); key_cx(kk[3], ee[3], kk[5], ee[5]);
+  key_cx(kk[1], ee[1], kk[2], ee[2]); key_cx(kk[3], ee[3], kk[4], ee[4]); key_cx(kk[5], ee[5], kk[6], ee[6]);
+  unsigned taken = 0u;  // bit i: this lane's expert lane + 32 i was picked
+  int my_e = 0;
+  float my_v = 0.f;
+  for (int r = 0; r < k; ++r) {
+    const uint32_t m = __reduce_max_sync(0xffffffffu, kk[0]);
+    const int emin = (int)__reduce_min_sync(0xffffffffu, (unsigned)(kk[0] == m ? ee[0] : 0x7fffffff));
+    if (ee[0] == emin) {
+      taken |= 1u << (emin >> 5);
+#pragma unroll
+      for (int i = 0; i < 7; ++i) {
+        kk[i] = kk[i + 1];
+        ee[i] = ee[i + 1];
+      }
+      kk[7] = 0u;
+      ee[7] = 0x7fffffff;
+    }
+    if (lane == r) {
+      my_e = emin < E ? emin : r;
+      my_v = key_value(m);
+    }
+  }
+  const bool finite = !(lane < k && !(my_v == my_v && my_v > -INFINITY));
+  const float vmax = __shfl_sync(0xffffffffu, my_v, 0);
+  const float ex = lane < k ? expf(my_v - vmax) : 0.f;
+  float den = ex;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
+  // rank by expert id: word[i] bit l <=> expert 32 i + l picked
+  unsigned word[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) word[i] = __ballot_sync(0xffffffffu, (taken >> i) & 1u);
+  const int wi = my_e >> 5, bi = my_e & 31;
+  int rank = 0;
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+    rank += (i < wi) ? __popc(word[i]) : ((i == wi) ? __popc(word[i] & ((1u << bi) - 1u)) : 0);
+  pick_e = my_e;
+  pick_w = ex / den;
+  pick_rank = rank;
+  return __all_sync(0xffffffffu, finite);
+}
 
 MOE_DEV uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));

@@ -115,25 +115,6 @@ __host__ __device__ inline size_t decode_big_bytes(const Shapes& s) {
   return a > b ? a : b;
 }
 
-// Order-preserving map of an fp32 value to u32 (NaN taken as -inf).
-MOE_DEV uint32_t ordered_key(float v) {
-  if (v != v) v = -INFINITY;
-  const uint32_t u = __float_as_uint(v);
-  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-}
-MOE_DEV float key_value(uint32_t k) { return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k); }
-
-// Compare-exchange of (value, id) pairs into descending value, ascending id.
-MOE_DEV void cx(uint32_t& ka, int& ea, uint32_t& kb, int& eb) {
-  const bool swap = (kb > ka) || (kb == ka && eb < ea);
-  const uint32_t tk = swap ? kb : ka, tk2 = swap ? ka : kb;
-  const int te = swap ? eb : ea, te2 = swap ? ea : eb;
-  ka = tk;
-  kb = tk2;
-  ea = te;
-  eb = te2;
-}
-
 // MAXT: compile-time bound on T (1 or 16), so the batch-1 kernel keeps one accumulator per lane.
 template <int NCH, int NCI, bool XBF16, int MAXT>
 __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const DecodeArgs A) {
@@ -242,71 +223,24 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const DecodeA
 
   // ---------------------------------------------------------------- phase B
   if (ok) {
-    // selection, identical in every block (same logits, same arithmetic):
-    // every lane sorts its 8 (logit, expert) pairs, then each of the k rounds
-    // takes the warp-wide largest head (ties to the lower expert id) with two
-    // warp reductions and pops it from its lane.
+    // selection, identical in every block (same logits, same arithmetic)
     if (warp < s.T) {
       const int t = warp;
-      uint32_t kk[8];
-      int ee[8];
+      float v[8];
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
         const int e = lane + 32 * i;
-        ee[i] = e;
-        kk[i] = (e < s.E) ? ordered_key(__ldcg(sc.logits + (size_t)t * s.E + e) + (A.rb ? A.rb[e] : 0.f)) : 0u;
+        v[i] = (e < s.E) ? __ldcg(sc.logits + (size_t)t * s.E + e) + (A.rb ? A.rb[e] : 0.f) : -INFINITY;
       }
-      // bitonic sorting network for 8 elements (descending key, ascending id)
-#define MOE_CX(i, j) cx(kk[i], ee[i], kk[j], ee[j])
-      MOE_CX(0, 1); MOE_CX(2, 3); MOE_CX(4, 5); MOE_CX(6, 7);
-      MOE_CX(0, 2); MOE_CX(1, 3); MOE_CX(4, 6); MOE_CX(5, 7);
-      MOE_CX(1, 2); MOE_CX(5, 6);
-      MOE_CX(0, 4); MOE_CX(1, 5); MOE_CX(2, 6); MOE_CX(3, 7);
-      MOE_CX(2, 4); MOE_CX(3, 5);
-      MOE_CX(1, 2); MOE_CX(3, 4); MOE_CX(5, 6);
-#undef MOE_CX
-      int my_e = 0;
-      float my_v = 0.f;
-      unsigned taken = 0u;  // bit i: this lane's expert lane + 32 i was picked
-      for (int r = 0; r < s.k; ++r) {
-        const uint32_t hk = kk[0];
-        const int he = (ee[0] < s.E) ? ee[0] : 0x7fffffff;
-        const uint32_t m = __reduce_max_sync(0xffffffffu, hk);
-        const int emin = (int)__reduce_min_sync(0xffffffffu, (unsigned)((hk == m) ? he : 0x7fffffff));
-        if (he == emin) {  // the winner pops its head
-          taken |= 1u << (he >> 5);
-#pragma unroll
-          for (int i = 0; i < 7; ++i) {
-            kk[i] = kk[i + 1];
-            ee[i] = ee[i + 1];
-          }
-          kk[7] = 0u;
-          ee[7] = 0x7fffffff;
-        }
-        if (lane == r) {
-          my_e = (emin < s.E) ? emin : r;
-          my_v = key_value(m);
-        }
-      }
-      if (lane < s.k && my_v != my_v) raise_status(A.ctl, kStatusBounds);
-      const float vmax = __shfl_sync(0xffffffffu, my_v, 0);
-      const float ex = lane < s.k ? expf(my_v - vmax) : 0.f;
-      const float den = warp_sum(ex);
-      // rank of every pick by expert id: word[i] bit l <=> expert 32 i + l picked
-      unsigned word[8];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) word[i] = __ballot_sync(0xffffffffu, (taken >> i) & 1u);
+      int pe, rank;
+      float pw;
+      if (!warp_top_k(v, s.E, s.k, lane, pe, pw, rank) && lane == 0) raise_status(A.ctl, kStatusBounds);
       if (lane < s.k) {
-        const int wi = my_e >> 5, bi = my_e & 31;
-        int rank = __popc(word[0] & ((wi > 0) ? 0xffffffffu : ((1u << bi) - 1u)));
-#pragma unroll
-        for (int i = 1; i < 8; ++i)
-          rank += (i < wi) ? __popc(word[i]) : ((i == wi) ? __popc(word[i] & ((1u << bi) - 1u)) : 0);
-        sel_e[t][rank] = my_e;
-        sel_w[t][rank] = ex / den;
+        sel_e[t][rank] = pe;
+        sel_w[t][rank] = pw;
         if (b == 0) {
-          sc.idx[(size_t)t * s.k + rank] = my_e;
-          sc.w[(size_t)t * s.k + rank] = ex / den;
+          sc.idx[(size_t)t * s.k + rank] = pe;
+          sc.w[(size_t)t * s.k + rank] = pw;
         }
       }
     }

@@ -178,85 +178,45 @@ cudaError_t launch_router_split_weights(const Shapes& s, const float* wr, const 
 }
 
 // ----------------------------------------------------------- selection
-// One block per chunk of 32 tokens, one warp per token at a time.  Each lane
-// holds the logits of experts lane, lane+32, ...; k rounds of a warp arg-max
-// (ties to the lower expert id) pick the experts.  The weights are
-// exp(l_j - l_max) / sum over the picked of exp(l - l_max): the full softmax
-// over all E experts renormalised over the picked ones, with the common
-// denominator cancelled.  The picks are written in ascending expert id, and
-// the chunk's per-expert token masks feed the grouping.
-__global__ void __launch_bounds__(256) select_kernel(Shapes s, const float* __restrict__ rb, int parts,
-                                                     Scratch sc, DevCtl ctl) {
+// One block per chunk of 32 tokens, one warp per token (warp_top_k: each
+// lane holds 8 logits; k rounds of warp reductions, ties to the lower expert
+// id).  The weights are the softmax over all E experts renormalised over the
+// picks; the picks are written in ascending expert id, and the chunk's
+// per-expert token masks feed the grouping.
+__global__ void __launch_bounds__(1024) select_kernel(Shapes s, const float* __restrict__ rb, int parts, Scratch sc,
+                                                      DevCtl ctl) {
   __shared__ unsigned mask[kMaxExperts];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int c = blockIdx.x, t0 = c * kChunk;
   const int nchunk = (s.T + kChunk - 1) / kChunk;
   for (int e = tid; e < s.E; e += blockDim.x) mask[e] = 0u;
   __syncthreads();
-  for (int tl = warp; tl < kChunk; tl += 8) {
-    const int t = t0 + tl;
-    if (t >= s.T) break;
+  const int t = t0 + warp;
+  if (t < s.T) {
     float v[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
       const int e = lane + 32 * i;
       float l = -INFINITY;
       if (e < s.E) {
+        const size_t te = (size_t)t * s.E + e;
         if (parts == 3) {  // tensor-core partial logits of the lo, mid and hi weight terms, small first
-          const size_t te = (size_t)t * s.E + e, part = (size_t)s.T * s.E;
+          const size_t part = (size_t)s.T * s.E;
           l = (sc.logits[2 * part + te] + sc.logits[part + te]) + sc.logits[te];
         } else {
-          l = sc.logits[(size_t)t * s.E + e];
+          l = sc.logits[te];
         }
         if (rb) l += rb[e];
       }
       v[i] = l;
     }
-    unsigned taken = 0u;
-    int my_e = 0;
-    float my_v = 0.f;
-    for (int r = 0; r < s.k; ++r) {
-      float bv = -INFINITY;
-      int bi = s.E;
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const int e = lane + 32 * i;
-        if (e < s.E && !(taken & (1u << i)) && (v[i] > bv || bi == s.E)) {
-          bv = v[i];
-          bi = e;
-        }
-      }
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-        const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-        if (oi < s.E && (bi >= s.E || ov > bv || (ov == bv && oi < bi))) {
-          bv = ov;
-          bi = oi;
-        }
-      }
-      if (bi >= s.E) {  // only reachable with NaN logits
-        if (lane == 0) raise_status(ctl, kStatusBounds);
-        bi = r;
-      }
-      if (lane == (bi & 31)) taken |= 1u << (bi >> 5);
-      if (lane == r) {
-        my_e = bi;
-        my_v = bv;
-      }
-    }
-    const float vmax = __shfl_sync(0xffffffffu, my_v, 0);
-    const float ex = lane < s.k ? expf(my_v - vmax) : 0.f;
-    const float den = warp_sum(ex);
-    int rank = 0;
-    for (int q = 0; q < s.k; ++q) {
-      const int oe = __shfl_sync(0xffffffffu, my_e, q);
-      rank += (oe < my_e) ? 1 : 0;
-    }
+    int pe, rank;
+    float pw;
+    if (!warp_top_k(v, s.E, s.k, lane, pe, pw, rank) && lane == 0) raise_status(ctl, kStatusBounds);
     if (lane < s.k) {
-      sc.idx[(size_t)t * s.k + rank] = my_e;
-      sc.w[(size_t)t * s.k + rank] = ex / den;
-      atomicOr(&mask[my_e], 1u << tl);
+      sc.idx[(size_t)t * s.k + rank] = pe;
+      sc.w[(size_t)t * s.k + rank] = pw;
+      atomicOr(&mask[pe], 1u << warp);
     }
   }
   __syncthreads();
@@ -270,7 +230,7 @@ __global__ void __launch_bounds__(256) select_kernel(Shapes s, const float* __re
 cudaError_t launch_select(const Shapes& s, const float* rb, int parts, const Scratch& sc, const DevCtl& ctl,
                           cudaStream_t st) {
   const int nchunk = (s.T + kChunk - 1) / kChunk;
-  select_kernel<<<nchunk, 256, 0, st>>>(s, rb, parts, sc, ctl);
+  select_kernel<<<nchunk, kChunk * 32, 0, st>>>(s, rb, parts, sc, ctl);
   return cudaGetLastError();
 }
 
