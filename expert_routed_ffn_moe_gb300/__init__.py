@@ -53,6 +53,10 @@ def lib() -> ctypes.CDLL:
         L.moe_set_path.argtypes = [P, I]
         L.moe_set_router.argtypes = [P, I]
         L.moe_set_spin_limit.argtypes = [P, ctypes.c_longlong]
+        L.moe_record_event.argtypes = [P, P]
+        L.moe_record_event.restype = I
+        L.moe_set_prefetch.argtypes = [P, P, P]
+        L.moe_set_prefetch.restype = I
         L.moe_inject_stall.argtypes = [P, I]
         L.moe_inject_stall.restype = I
         L.moe_time_kernel.argtypes = [P, I, P, P]
@@ -133,6 +137,16 @@ def moe_set_router(ctx, router: int) -> None:
 
 def moe_set_spin_limit(ctx, limit_ns: int) -> None:
     _check(lib().moe_set_spin_limit(ctx, limit_ns), "moe_set_spin_limit")
+
+
+def moe_record_event(event, stream=None) -> None:
+    """Record a torch.cuda.Event on a stream; timeable also under graph capture."""
+    _check(lib().moe_record_event(ctypes.c_void_p(event.cuda_event), _stream(stream)), "moe_record_event")
+
+
+def moe_set_prefetch(ctx, next_router_w=None, next_shared_w=None) -> None:
+    """Hint: the next small-T forward pulls these next-layer weights into L2."""
+    _check(lib().moe_set_prefetch(ctx, _ptr(next_router_w), _ptr(next_shared_w)), "moe_set_prefetch")
 
 
 def moe_inject_stall(ctx, on: bool) -> None:

@@ -23,6 +23,8 @@ struct moe_ctx {
   int router = MOE_ROUTER_AUTO;
   long long spin_ns = 0;
   int stall = 0;            // test hook (moe_inject_stall)
+  const float* next_wr = nullptr;         // prefetch hint for the next call (moe_set_prefetch)
+  const uint16_t* next_shared = nullptr;
   int gemv_max_t = 0;       // largest T the GEMV kernels accept for this shape (0: none)
   int decode_max_t = 0;     // largest T the fused decode kernel accepts (0: none)
   void* block = nullptr;    // the single device allocation holding all scratch
@@ -38,6 +40,7 @@ namespace {
 
 constexpr long long kDefaultSpinNs = 1000000000LL;  // 1 s
 constexpr int kGemvSmemLimit = 200 * 1024;           // dynamic shared memory of the GEMV kernels
+constexpr int kDecodeReps = 8;                       // copies of the decode kernel's broadcast data
 
 int cuda_fail(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
 
@@ -199,7 +202,7 @@ int moe_init(const moe_config* cfg, moe_ctx** out) {
   if (!(prop.major == 10 && prop.minor == 3)) return MOE_ERR_UNSUPPORTED;
 
   if (prepare_gemm_kernels() != cudaSuccess || prepare_gemv_kernels(kGemvSmemLimit) != cudaSuccess ||
-      prepare_decode_kernels(kGemvSmemLimit) != cudaSuccess) {
+      prepare_decode_kernels(kDecodeSmemLimit) != cudaSuccess) {
     cudaGetLastError();
     return MOE_ERR_CUDA;
   }
@@ -220,7 +223,7 @@ int moe_init(const moe_config* cfg, moe_ctx** out) {
     s1.k = c.top_k;
     s1.has_shared = c.has_shared;
     s1.x_bf16 = c.x_dtype == MOE_BF16;
-    if (decode_supported(s1, kGemvSmemLimit) && decode_blocks_per_sm(s1) >= 1) ctx->decode_max_t = t;
+    if (decode_supported(s1, kDecodeSmemLimit) && decode_blocks_per_sm(s1, kDecodeSmemLimit) >= 1) ctx->decode_max_t = t;
   }
 
   void* fn = nullptr;
@@ -264,7 +267,10 @@ int moe_init(const moe_config* cfg, moe_ctx** out) {
   const size_t o_hg = take(tg ? (tg * k + tg) * I * 4 : 16);
   const size_t o_out = take(rows * d * 2);
   const size_t o_status = take(16);
-  const size_t o_gridbar = take(16);
+  const size_t o_gridbar = take(64);
+  const size_t o_dlog = take(ctx->decode_max_t ? (size_t)kDecodeReps * ctx->decode_max_t * E * 8 : 16);
+  const size_t dpairs = (size_t)ctx->decode_max_t * (k + 1);
+  const size_t o_dh = take(ctx->decode_max_t ? (size_t)kDecodeReps * dpairs * I * 8 : 16);
   if (cudaMalloc(&ctx->block, off) != cudaSuccess) {
     cudaGetLastError();
     delete ctx;
@@ -297,6 +303,10 @@ int moe_init(const moe_config* cfg, moe_ctx** out) {
   sc.out = reinterpret_cast<uint16_t*>(b + o_out);
   sc.status = reinterpret_cast<unsigned*>(b + o_status);
   sc.gridbar = reinterpret_cast<unsigned*>(b + o_gridbar);
+  sc.dec_logits = reinterpret_cast<float*>(b + o_dlog);
+  sc.dec_h = reinterpret_cast<float*>(b + o_dh);
+  sc.dec_reps = kDecodeReps;
+  sc.dec_hreps = kDecodeReps;
   sc.max_mtiles = max_mtiles;
   *out = ctx;
   return MOE_OK;
@@ -317,6 +327,20 @@ int moe_set_router(moe_ctx* ctx, int router) {
 int moe_set_spin_limit(moe_ctx* ctx, long long limit) {
   if (!ctx || limit < 0) return MOE_ERR_ARG;
   ctx->spin_ns = limit == 0 ? kDefaultSpinNs : limit;
+  return MOE_OK;
+}
+
+int moe_record_event(void* event, void* stream) {
+  if (!event) return MOE_ERR_ARG;
+  return cuda_fail(record_event(static_cast<cudaEvent_t>(event), static_cast<cudaStream_t>(stream)));
+}
+
+int moe_set_prefetch(moe_ctx* ctx, const float* next_router_w, const void* next_shared_w) {
+  if (!ctx) return MOE_ERR_ARG;
+  if ((next_router_w && !aligned16(next_router_w)) || (next_shared_w && !aligned16(next_shared_w)))
+    return MOE_ERR_ALIGN;
+  ctx->next_wr = next_router_w;
+  ctx->next_shared = static_cast<const uint16_t*>(next_shared_w);
   return MOE_OK;
 }
 
@@ -384,8 +408,10 @@ int moe_forward(moe_ctx* ctx, const void* x, int T, const float* router_w, const
     // the whole layer in one cooperative launch
     const cudaError_t err = launch(ctx, MOE_K_DECODE_FUSED, st, [&] {
       return launch_decode_fused(s, x, router_w, router_b, gu, dn, sw, y, ctx->sc, ctl, ctx->sc.gridbar,
-                                 ctx->num_sms, st);
+                                 ctx->num_sms, st, ctx->next_wr, ctx->next_shared, kDecodeSmemLimit);
     });
+    ctx->next_wr = nullptr;  // a hint serves one call
+    ctx->next_shared = nullptr;
     return cuda_fail(err);
   }
   if (path == MOE_PATH_GEMV) {
@@ -434,8 +460,9 @@ int moe_status(moe_ctx* ctx) {
   unsigned v = 0;
   if (cudaMemcpy(&v, ctx->sc.status, 4, cudaMemcpyDeviceToHost) != cudaSuccess) return MOE_ERR_CUDA;
   if (v && cudaMemset(ctx->sc.status, 0, 4) != cudaSuccess) return MOE_ERR_CUDA;
-  // a kernel that gave up may have left the grid-barrier counters mid-way
-  if ((v & kStatusTimeout) && cudaMemset(ctx->sc.gridbar, 0, 8) != cudaSuccess) return MOE_ERR_CUDA;
+  // nothing to repair after a timeout: every block of a decode launch that gave
+  // up still leaves through the exit counter, and the next launch tags its
+  // values with a new epoch, so nothing the failed launch wrote is taken as ready
   if (v & kStatusTimeout) return MOE_ERR_TIMEOUT;
   if (v & kStatusBounds) return MOE_ERR_BOUNDS;
   return MOE_OK;

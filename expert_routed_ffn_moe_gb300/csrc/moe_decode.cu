@@ -1,6 +1,6 @@
 // Fused decode layer: the whole MoE layer for a handful of tokens in ONE
 // cooperative persistent kernel (one block per SM), three phases separated by
-// two grid barriers.
+// two grid-wide data dependencies.
 //
 // "Optimizing on-device inference for Apple Silicon", section "Decoding:
 // minimize bytes moved per token": at batch 1 throughput is set by the bytes
@@ -12,23 +12,34 @@
 // independent GPU work": a barrier only where later work needs an earlier
 // result.  Section "Keeping each decode step on the GPU": no host round trip.
 //
-//   phase A  router logits l[t, e] (fp32 FMA, one block per expert pair, the
-//            row split over 8 warps and summed in a fixed order); meanwhile the
-//            shared expert's weights (routing-independent) are prefetched into L2.
-//   -- grid barrier --
-//   phase B  every block selects the top-k of every token from the logits (same
-//            result in every block), groups tokens by expert in shared memory,
-//            prefetches into L2 every weight row it will read in phases B and C,
-//            then runs the gate/up GEMV + SwiGLU for its (expert, neuron) units.
-//   -- grid barrier --
+//   phase A  router logits l[t, e] (fp32 FMA, four experts per pass, each row
+//            split over 4 warps and summed in a fixed order), and the shared
+//            expert's gate/up GEMV + SwiGLU, which needs no routing.
+//   -- every block waits for all logits --
+//   phase B  every block selects the top-k of every token from the logits
+//            (one warp per token; same result in every block); groups tokens
+//            by expert in shared memory; runs the routed gate/up GEMV +
+//            SwiGLU for its (expert, neuron) units; then loads its phase-C
+//            down rows.
+//   -- every block waits for all of h --
 //   phase C  one warp per output feature: for the active experts in ascending
-//            id (shared expert last) the down-projection row from L2, dotted
-//            with each routed token's h, scaled by its routing weight, summed
-//            per token in fp32 and written to y.
+//            id (shared expert last) the down-projection row, dotted with each
+//            routed token's h, scaled by its routing weight, summed per token
+//            in fp32 and written to y.
+// h is written in several copies and block b reads copy b mod copies, so that
+// no L2 line is read by every SM at once.
 //
-// Barriers are counter barriers with a bounded spin (MOE_ERR_TIMEOUT); the last
-// block to leave resets the counters, so graph replays start from zero.
+// The two waits are not barriers: every logit and every h value is published
+// as a 64-bit word holding the value and the launch's epoch, and a reader
+// polls the words it needs until all carry the current epoch (bounded spin,
+// MOE_ERR_TIMEOUT).  Data and readiness travel in one access, so a block
+// starts on the logits one L2 round trip after the last of them lands, instead
+// of after a barrier's arrive, poll and release and then a separate load.  The
+// last block to leave publishes the launch's epoch; the next launch, a graph
+// replay included, tags with the one after it.
 #include <math.h>
+
+#include <mutex>
 
 #include "moe_internal.h"
 
@@ -37,54 +48,62 @@ namespace moe {
 namespace {
 
 constexpr int kWarps = 16;
+constexpr int kRowChunks = 4;                    // warps sharing one router row
+constexpr int kSlots = kWarps / kRowChunks;      // router rows per pass
 constexpr int kThreads = kWarps * 32;
+constexpr int kMaxSlots = 32;                    // TMA ring slots (upper bound)
 
 MOE_DEV void prefetch_l2(const void* p, uint32_t bytes) {
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(p)), "r"(bytes)
                : "memory");
 }
-MOE_DEV unsigned ld_acquire(const unsigned* p) {
+MOE_DEV unsigned ld_relaxed(const unsigned* p) {
   unsigned v;
-  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
   return v;
 }
 
-// Arrive at grid barrier `n` (1-based) and wait for every block; false on timeout.
-MOE_DEV bool grid_sync(unsigned* count, unsigned n, const DevCtl& c, int* flag) {
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    int ok = 1;
-    __threadfence();
-    atomicAdd(count, 1u);
-    // test hook: wait for one arrival more than there are blocks (never happens)
-    const unsigned target = n * gridDim.x + (c.stall ? 1u : 0u);
-    const long long t0 = clock64(), lim = wait_cycles(c);
-    while (ld_acquire(count) < target) {
-      if (clock64() - t0 > lim) {
-        raise_status(c, kStatusTimeout);
-        ok = 0;
-        break;
-      }
-    }
-    __threadfence();
-    *flag = ok;
-  }
-  __syncthreads();
-  return *flag != 0;
+// Values that one block produces and every other block consumes (the router
+// logits, the SwiGLU activations h) carry the launch's epoch in the high half
+// of the same 64-bit word.  A reader polls the word itself until the tag
+// matches, so no separate barrier or flag is needed: the payload and its
+// readiness arrive in one single-copy-atomic access.
+MOE_DEV void st_tagged(unsigned long long* p, float v, unsigned ep) {
+  const unsigned long long w = ((unsigned long long)ep << 32) | __float_as_uint(v);
+  asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(w) : "memory");
 }
+// (volatile, so every poll re-reads; no memory clobber, so independent polls
+// issue back to back)
+MOE_DEV unsigned long long ld_tagged(const unsigned long long* p) {
+  unsigned long long w;
+  asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(w) : "l"(p));
+  return w;
+}
+MOE_DEV void ld_tagged2(const unsigned long long* p, unsigned long long& a, unsigned long long& b) {
+  asm volatile("ld.relaxed.gpu.global.v2.u64 {%0, %1}, [%2];" : "=l"(a), "=l"(b) : "l"(p));
+}
+MOE_DEV unsigned tag_of(unsigned long long w) { return (unsigned)(w >> 32); }
+MOE_DEV float value_of(unsigned long long w) { return __uint_as_float((unsigned)w); }
 
-MOE_DEV float dot8(const uint4 w, const float* x) {
-  const float4 a = *reinterpret_cast<const float4*>(x);
-  const float4 b = *reinterpret_cast<const float4*>(x + 4);
-  float s = bf16_lo(w.x) * a.x;
+// Dot products over 4 consecutive elements: an 8-byte chunk of bf16 weights
+// against one float4 of activations.  A lane takes chunk lane + 32 c, so a
+// warp reads 256 contiguous weight bytes and 512 contiguous activation bytes
+// per step: no shared-memory bank conflicts on either side.
+MOE_DEV void dot4x2(const uint2 g, const uint2 u, const float4 a, float& gs, float& us) {
+  gs = fmaf(bf16_lo(g.x), a.x, gs);
+  us = fmaf(bf16_lo(u.x), a.x, us);
+  gs = fmaf(bf16_hi(g.x), a.y, gs);
+  us = fmaf(bf16_hi(u.x), a.y, us);
+  gs = fmaf(bf16_lo(g.y), a.z, gs);
+  us = fmaf(bf16_lo(u.y), a.z, us);
+  gs = fmaf(bf16_hi(g.y), a.w, gs);
+  us = fmaf(bf16_hi(u.y), a.w, us);
+}
+MOE_DEV float dot4(const uint2 w, const float4 a, float s) {
+  s = fmaf(bf16_lo(w.x), a.x, s);
   s = fmaf(bf16_hi(w.x), a.y, s);
   s = fmaf(bf16_lo(w.y), a.z, s);
-  s = fmaf(bf16_hi(w.y), a.w, s);
-  s = fmaf(bf16_lo(w.z), b.x, s);
-  s = fmaf(bf16_hi(w.z), b.y, s);
-  s = fmaf(bf16_lo(w.w), b.z, s);
-  s = fmaf(bf16_hi(w.w), b.w, s);
-  return s;
+  return fmaf(bf16_hi(w.y), a.w, s);
 }
 
 }  // namespace
@@ -100,8 +119,94 @@ struct DecodeArgs {
   void* y;
   Scratch sc;
   DevCtl ctl;
-  unsigned* bar;   // [0] arrivals, [1] departures
+  unsigned* bar;   // [0] exit counter, [1] epoch of the last launch
+  // optional prefetch hint: weights the next layer reads first (may be null)
+  const float* next_wr;
+  const uint16_t* next_shared;
+  int ring_slots;     // S: slots of the weight ring in shared memory (2..kMaxSlots)
+  int slot_bytes;     // bytes per slot: max(gate + up row, chunk_experts down rows)
+  int chunk_experts;  // down-projection rows (one per active expert) per slot
 };
+
+MOE_DEV void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::"r"(
+          smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
+      : "memory");
+}
+MOE_DEV void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
+// Start the bulk copies of item q of this block's weight stream into `slot`
+// (one thread).  Items q < n_sh are the shared expert's gate/up units
+// i = b + q G: its gate row i and up row i, back to back.  The next nu items
+// are routed gate/up units u = b + q' G (q' = q - n_sh): the gate and up rows
+// of neuron i of active expert a.  Later items are chunks of phase-C rows: for
+// output row r = b + j G, the down-projection rows r of active experts
+// a0 .. a0 + na - 1, back to back.
+MOE_DEV void issue_item(const DecodeArgs& A, int q, int slot, int n_sh, int nu, int nch, int b, int G, int n_act,
+                        const int* act_e, uint8_t* ring, uint64_t* full, int* slot_issued) {
+  const Shapes& s = A.s;
+  uint8_t* dst = ring + (size_t)slot * A.slot_bytes;
+  const uint64_t pol = policy_evict_first();
+  if (q < n_sh) {
+    const int i = b + q * G;
+    const uint32_t row = (uint32_t)s.d * 2;
+    mbar_expect_tx(&full[slot], 2 * row);
+    bulk_g2s(dst, A.shared_w + (size_t)i * s.d, row, &full[slot], pol);
+    bulk_g2s(dst + row, A.shared_w + (size_t)(s.I + i) * s.d, row, &full[slot], pol);
+  } else if ((q -= n_sh) < nu) {
+    const int u = b + q * G, a = u / s.I, i = u - a * s.I;
+    const uint16_t* W = A.gate_up + (size_t)act_e[a] * 2 * s.I * s.d;
+    const uint32_t row = (uint32_t)s.d * 2;
+    mbar_expect_tx(&full[slot], 2 * row);
+    bulk_g2s(dst, W + (size_t)i * s.d, row, &full[slot], pol);
+    bulk_g2s(dst + row, W + (size_t)(s.I + i) * s.d, row, &full[slot], pol);
+  } else {
+    const int m = q - nu, j = m / nch, c = m - j * nch;
+    const int r = b + j * G, a0 = c * A.chunk_experts, na = min(A.chunk_experts, n_act - a0);
+    const uint32_t row = (uint32_t)s.I * 2;
+    mbar_expect_tx(&full[slot], (uint32_t)na * row);
+    for (int qa = 0; qa < na; ++qa) {
+      const int e = act_e[a0 + qa];
+      const uint16_t* Wd = (e < s.E) ? A.down + (size_t)e * s.d * s.I : A.shared_w + (size_t)2 * s.I * s.d;
+      bulk_g2s(dst + (size_t)qa * row, Wd + (size_t)r * s.I, row, &full[slot], pol);
+    }
+  }
+  __threadfence_block();
+  volatile int* issued = slot_issued + slot;
+  *issued = *issued + 1;  // read by other warps' wait_item
+}
+
+// Wait until item q of the weight stream has landed in its slot q mod S.  An
+// mbarrier's parity names a phase only up to two: a consumer that reached
+// item q while the slot still held item q - S in flight would see the parity
+// it waits for already flipped.  So the consumer first waits until item q has
+// been issued (slot_issued[slot] > q / S); items are issued into a slot only
+// after the previous one there was consumed, so from then on the parity is
+// unambiguous.  Bounded like every wait (false and MOE_ERR_TIMEOUT latched).
+MOE_DEV bool wait_item(uint64_t* full, const int* slot_issued, int q, int S, const DevCtl& c) {
+  const int slot = q % S, use = q / S;
+  const volatile int* issued = slot_issued + slot;
+  if (*issued <= use) {
+    const long long t0 = clock64(), lim = wait_cycles(c);
+    for (int polls = 1; *issued <= use; ++polls) {
+      if (polls >= 256 && clock64() - t0 > lim) {
+        raise_status(c, kStatusTimeout);
+        return false;
+      }
+    }
+  }
+  return mbar_wait(&full[slot], (uint32_t)use & 1u, c);
+}
+
+// A slot holds at most one item in flight (the next is issued only after the
+// previous one was waited for), so waiting for the parity of the last issued
+// item of the slot waits for everything still in flight there.
+MOE_DEV void drain_slot(uint64_t* full, const int* slot_issued, int slot, const DevCtl& c) {
+  const int m = slot_issued[slot];
+  if (m > 0) mbar_wait(&full[slot], (uint32_t)(m - 1) & 1u, c);
+}
 
 // Shared-memory layout (bytes from the dynamic base).
 struct DecodeSmem {
@@ -123,42 +228,64 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const DecodeA
   const Scratch& sc = A.sc;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, tid = threadIdx.x;
   const int G = gridDim.x, b = blockIdx.x;
+  const int tk = s.T * s.k;
+  const size_t pairs = (size_t)tk + (s.has_shared ? s.T : 0);
+  const size_t hrep = pairs * s.I;  // floats per copy of h
 
-  float* big = reinterpret_cast<float*>(dsm);
-  __shared__ float rpart[2][8][16];        // router partial sums [slot][chunk][token]
-  __shared__ int sel_e[16][kMaxTopK];      // chosen experts per token, ascending
-  __shared__ float sel_w[16][kMaxTopK];
-  __shared__ int act_e[kMaxExperts + 1];   // active experts ascending, shared last
+  float* big = reinterpret_cast<float*>(dsm);  // x as fp32 [T][d] (phases A, B), then h [pairs][I] (phase C)
+  __shared__ float rpart[kSlots][kRowChunks][MAXT];  // router partial sums [slot][chunk][token]
+  __shared__ int sel_e[MAXT][kMaxTopK];         // picks per token, ascending expert id
+  __shared__ float sel_w[MAXT][kMaxTopK];       // their weights
+  __shared__ int act_e[kMaxExperts + 1];        // active experts ascending, shared last
   __shared__ unsigned act_m[kMaxExperts + 1];
-  __shared__ int act_row[kMaxExperts + 1]; // first grouped h row of each active expert
-  __shared__ float act_w[kMaxExperts + 1][16];  // routing weight of each token for the expert
+  __shared__ int act_row[kMaxExperts + 1];      // first grouped h row of each active expert
+  __shared__ float act_w[kMaxExperts + 1][MAXT];
   __shared__ int n_act_s, flag_s;
+  __shared__ unsigned ep_s;  // this launch's epoch: the tag of every value it publishes
   __shared__ int warp_tot[kWarps];
+  __shared__ __align__(8) uint64_t full[kMaxSlots];  // ring slot filled (TMA transaction count)
+  __shared__ int slot_issued[kMaxSlots];             // items issued into each slot so far
+  uint8_t* const ring = dsm + decode_big_bytes(s);   // A.ring_slots x A.slot_bytes
+  int n_items = 0;                                   // this block's weight items (phases B and C)
+  const int n_sh = s.has_shared ? ((s.I > b) ? (s.I - b + G - 1) / G : 0) : 0;  // shared-expert units
 
+  if (tid == 0) {
+    const unsigned e = ld_relaxed(A.bar + 1) + 1u;  // the previous launch's epoch + 1 (0 is never a tag)
+    ep_s = e ? e : 1u;
+    flag_s = 1;
+    for (int i = 0; i < A.ring_slots; ++i) {
+      mbar_init(&full[i], 1);
+      slot_issued[i] = 0;
+    }
+    fence_mbar_init();
+  }
+  unsigned long long* const dlog = reinterpret_cast<unsigned long long*>(sc.dec_logits);
+  unsigned long long* const dh = reinterpret_cast<unsigned long long*>(sc.dec_h);
   bool ok = true;
   // ---------------------------------------------------------------- phase A
+  // router logits, and the shared expert's gate/up GEMV (it needs no routing)
   {
-    // router rows first (they need nothing), then x; lane owns NCH consecutive
-    // columns of its warp's d/8-wide chunk
-    constexpr int kPer = NCH;  // = d / 256
-    const int chunk = s.d / 8;
-    const int slot = warp >> 3, cw = warp & 7;
-    const int col0 = cw * chunk + lane * kPer;
-    float wv[1][kPer];
-    int n_e0 = 0;
-    for (int e0 = b; e0 < s.E; e0 += 2 * G) ++n_e0;
+    // a warp covers a d/4-wide quarter of a router row; its lane takes the
+    // float4 columns lane + 32 i of that quarter (coalesced weight loads,
+    // conflict-free x reads)
+    constexpr int kPer4 = NCH / 2;  // = d / 512: float4 per lane
+    const int chunk = s.d / kRowChunks;
+    const int slot = warp / kRowChunks, cw = warp % kRowChunks;
+    const int col0 = cw * chunk;
+    float4 rw[kPer4];
     {
       const int e = b + slot * G;
       if (e < s.E) {
-        const float2* wrow = reinterpret_cast<const float2*>(A.wr + (size_t)e * s.d + col0);
+        const float4* wrow = reinterpret_cast<const float4*>(A.wr + (size_t)e * s.d + col0) + lane;
 #pragma unroll
-        for (int i = 0; i < kPer / 2; ++i) {
-          const float2 v = __ldg(wrow + i);
-          wv[0][2 * i] = v.x;
-          wv[0][2 * i + 1] = v.y;
-        }
+        for (int i = 0; i < kPer4; ++i) rw[i] = __ldg(wrow + 32 * i);
       }
     }
+    // this block's shared-expert neurons i = b + q G (items q < n_sh of the
+    // weight stream) start streaming into the ring now: they need no routing
+    if (tid == 0)
+      for (int q = 0; q < n_sh && q < A.ring_slots; ++q)
+        issue_item(A, q, q, n_sh, 0, 1, b, G, 0, nullptr, ring, full, slot_issued);
     const int nx = s.T * s.d;
     if (XBF16) {
       const uint32_t* xb = static_cast<const uint32_t*>(A.x);
@@ -171,66 +298,116 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const DecodeA
       const float2* xf = static_cast<const float2*>(A.x);
       for (int i = tid; i < nx / 2; i += kThreads) reinterpret_cast<float2*>(big)[i] = __ldg(xf + i);
     }
-    // the shared expert does not depend on routing: pull its weights into L2 now
-    if (s.has_shared) {
-      const size_t bytes = (size_t)3 * s.I * s.d * 2;
-      const size_t per = ((bytes / G) + 4095) & ~size_t(4095);
-      const size_t lo = per * b, hi = min(bytes, lo + per);
-      const uint8_t* base = reinterpret_cast<const uint8_t*>(A.shared_w);
-      for (size_t off = lo + (size_t)tid * 4096; off < hi; off += (size_t)kThreads * 4096)
-        prefetch_l2(base + off, (uint32_t)min((size_t)4096, hi - off));
-    }
     __syncthreads();
+    int n_e0 = 0;
+    for (int e0 = b; e0 < s.E; e0 += kSlots * G) ++n_e0;
     for (int rep = 0; rep < n_e0; ++rep) {
-      const int e = b + rep * 2 * G + slot * G;
+      const int e = b + rep * kSlots * G + slot * G;
       if (rep > 0 && e < s.E) {
-        const float2* wrow = reinterpret_cast<const float2*>(A.wr + (size_t)e * s.d + col0);
+        const float4* wrow = reinterpret_cast<const float4*>(A.wr + (size_t)e * s.d + col0) + lane;
 #pragma unroll
-        for (int i = 0; i < kPer / 2; ++i) {
-          const float2 v = __ldg(wrow + i);
-          wv[0][2 * i] = v.x;
-          wv[0][2 * i + 1] = v.y;
-        }
+        for (int i = 0; i < kPer4; ++i) rw[i] = __ldg(wrow + 32 * i);
       }
       if (e < s.E) {
 #pragma unroll
         for (int t = 0; t < MAXT; ++t) {
           if (t < s.T) {
-            const float* xr = big + (size_t)t * s.d + col0;
+            const float4* xr = reinterpret_cast<const float4*>(big + (size_t)t * s.d + col0) + lane;
             float acc = 0.f;
 #pragma unroll
-            for (int i = 0; i < kPer; ++i) acc = fmaf(wv[0][i], xr[i], acc);
+            for (int i = 0; i < kPer4; ++i) {
+              const float4 xv = xr[32 * i];
+              acc = fmaf(rw[i].x, xv.x, acc);
+              acc = fmaf(rw[i].y, xv.y, acc);
+              acc = fmaf(rw[i].z, xv.z, acc);
+              acc = fmaf(rw[i].w, xv.w, acc);
+            }
             acc = warp_sum(acc);
             if (lane == 0) rpart[slot][cw][t] = acc;
           }
         }
       }
       __syncthreads();
-      if (tid < 2 * 16) {
-        const int sl = tid >> 4, t = tid & 15;
-        const int ee = b + rep * 2 * G + sl * G;
+      // every block reads all logits in phase B: write dec_reps copies so
+      // that the reads spread over several L2 lines instead of one hot set
+      for (int q = tid; q < kSlots * MAXT * sc.dec_reps; q += kThreads) {
+        const int sl = q % kSlots, t = (q / kSlots) % MAXT, r = q / (kSlots * MAXT);
+        const int ee = b + rep * kSlots * G + sl * G;
         if (ee < s.E && t < s.T) {
           float l = 0.f;
 #pragma unroll
-          for (int c = 0; c < 8; ++c) l += rpart[sl][c][t];
-          sc.logits[(size_t)t * s.E + ee] = l;
+          for (int c = 0; c < kRowChunks; ++c) l += rpart[sl][c][t];
+          st_tagged(dlog + ((size_t)r * s.T + t) * s.E + ee, l, ep_s);
         }
       }
       __syncthreads();
     }
+    // shared-expert gate/up + SwiGLU: item q < n_sh goes to warp q mod kWarps
+    for (int q = warp; q < n_sh; q += kWarps) {
+      const int slot = q % A.ring_slots;
+      if (!wait_item(full, slot_issued, q, A.ring_slots, A.ctl)) {
+        flag_s = 0;
+        break;
+      }
+      const int i = b + q * G;
+      const uint2* grow = reinterpret_cast<const uint2*>(ring + (size_t)slot * A.slot_bytes) + lane;
+      const uint2* urow = grow + s.d / 4;
+      for (int t = 0; t < s.T; ++t) {
+        const float4* xr = reinterpret_cast<const float4*>(big + (size_t)t * s.d) + lane;
+        float g = 0.f, up = 0.f;
+#pragma unroll
+        for (int c = 0; c < 2 * NCH; ++c) dot4x2(grow[32 * c], urow[32 * c], xr[32 * c], g, up);
+        g = warp_sum(g);
+        up = warp_sum(up);
+        if (lane < sc.dec_hreps) st_tagged(dh + (size_t)lane * hrep + ((size_t)tk + t) * s.I + i, silu(g) * up, ep_s);
+      }
+      __syncwarp();  // every lane has read the slot
+      if (lane == 0 && q + A.ring_slots < n_sh) {  // later items need the routing: phase B issues them
+        fence_proxy_async_smem();
+        issue_item(A, q + A.ring_slots, slot, n_sh, 0, 1, b, G, 0, nullptr, ring, full, slot_issued);
+      }
+    }
   }
-  ok = grid_sync(A.bar, 1, A.ctl, &flag_s);
 
   // ---------------------------------------------------------------- phase B
-  if (ok) {
-    // selection, identical in every block (same logits, same arithmetic)
-    if (warp < s.T) {
-      const int t = warp;
+  // selection, identical in every block (same logits, same arithmetic); the
+  // logits are polled until every one carries this launch's tag
+  {
+    const unsigned long long* logits = dlog + (size_t)(b % sc.dec_reps) * s.T * s.E;
+    // test hook: wait for a tag that no block writes
+    const unsigned want = ep_s + (A.ctl.stall ? 1u : 0u);
+    for (int t = warp; t < s.T; t += kWarps) {
       float v[8];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const int e = lane + 32 * i;
-        v[i] = (e < s.E) ? __ldcg(sc.logits + (size_t)t * s.E + e) + (A.rb ? A.rb[e] : 0.f) : -INFINITY;
+      for (int i = 0; i < 8; ++i) v[i] = (A.rb && lane + 32 * i < s.E) ? __ldg(A.rb + lane + 32 * i) : 0.f;
+      const long long t0 = clock64(), lim = wait_cycles(A.ctl);
+      bool late = false;
+      for (int polls = 1;; ++polls) {
+        // all eight words are loaded before any is tested: a load that waited
+        // on the previous one's tag would make the poll eight round trips long
+        unsigned long long w[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          w[i] = (lane + 32 * i < s.E) ? ld_tagged(logits + (size_t)t * s.E + lane + 32 * i) : 0ull;
+        bool ready = true;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) ready = ready && (lane + 32 * i >= s.E || tag_of(w[i]) == want);
+        if (__all_sync(0xffffffffu, ready)) {
+#pragma unroll
+          for (int i = 0; i < 8; ++i) v[i] = (lane + 32 * i < s.E) ? value_of(w[i]) + v[i] : -INFINITY;
+          break;
+        }
+        if (polls >= 256 && __any_sync(0xffffffffu, clock64() - t0 > lim)) {
+          late = true;
+          break;
+        }
+      }
+      if (late) {
+        if (lane == 0) {
+          raise_status(A.ctl, kStatusTimeout);
+          flag_s = 0;
+        }
+        continue;
       }
       int pe, rank;
       float pw;
@@ -244,7 +421,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const DecodeA
         }
       }
     }
-    __syncthreads();
+  }
+  __syncthreads();
+  ok = flag_s != 0;
+  if (ok) {
     // group tokens by expert: masks, active list (ascending), grouped h rows
     unsigned m = 0u;
     if (tid < s.E) {
@@ -254,8 +434,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const DecodeA
     }
     {
       const int flag = (tid < s.E && m) ? 1 : 0, cnt = (tid < s.E) ? __popc(m) : 0;
-      // block scan of (flag, cnt) packed: flag in the high half, count in the low half
-      int v = (flag << 16) | cnt, incl = v;
+      int v = (flag << 16) | cnt, incl = v;  // flag count in the high half, rows in the low half
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
         const int n = __shfl_up_sync(0xffffffffu, incl, o);
@@ -271,10 +450,11 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const DecodeA
         act_e[pos] = tid;
         act_m[pos] = m;
         act_row[pos] = excl & 0xffff;
-        for (int t = 0; t < s.T; ++t) {
+        for (int t = 0; t < MAXT; ++t) {
           float wt = 0.f;
-          for (int j = 0; j < s.k; ++j)
-            if (sel_e[t][j] == tid) wt = sel_w[t][j];
+          if (t < s.T)
+            for (int j = 0; j < s.k; ++j)
+              if (sel_e[t][j] == tid) wt = sel_w[t][j];
           act_w[pos][t] = wt;
         }
       }
@@ -285,99 +465,131 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const DecodeA
         if (s.has_shared) {
           act_e[n_routed] = s.E;
           act_m[n_routed] = (s.T >= 32) ? 0xffffffffu : ((1u << s.T) - 1u);
-          act_row[n_routed] = s.T * s.k;
-          for (int t = 0; t < s.T; ++t) act_w[n_routed][t] = 1.f;
+          act_row[n_routed] = tk;
+          for (int t = 0; t < MAXT; ++t) act_w[n_routed][t] = t < s.T ? 1.f : 0.f;
         }
         n_act_s = n_routed + (s.has_shared ? 1 : 0);
       }
     }
     __syncthreads();
     const int n_act = n_act_s;
-    const int units = n_act * s.I;
-    const size_t row_bytes = (size_t)s.d * 2, drow_bytes = (size_t)s.I * 2;
-    // L2 prefetch of everything this block reads in phases B and C, so the
-    // memory system sees all of it at once
-    {
-      const int my_units = (units > b) ? (units - b + G - 1) / G : 0;
-      for (int q = tid; q < 2 * my_units; q += kThreads) {
-        const int u = b + (q >> 1) * G;
-        const int a = u / s.I, i = u - a * s.I;
-        const int e = act_e[a];
-        const uint16_t* W = (e < s.E) ? A.gate_up + (size_t)e * 2 * s.I * s.d : A.shared_w;
-        prefetch_l2(W + (size_t)((q & 1) ? s.I + i : i) * s.d, (uint32_t)row_bytes);
-      }
-      const int my_rows = (s.d > b) ? (s.d - b + G - 1) / G : 0;
-      for (int q = tid; q < my_rows * n_act; q += kThreads) {
-        const int r = b + (q / n_act) * G, a = q % n_act;
-        const int e = act_e[a];
-        const uint16_t* Wd = (e < s.E) ? A.down + (size_t)e * s.d * s.I : A.shared_w + (size_t)2 * s.I * s.d;
-        prefetch_l2(Wd + (size_t)r * s.I, (uint32_t)drow_bytes);
-      }
+    const int n_routed = n_act - (s.has_shared ? 1 : 0);
+    const int units = n_routed * s.I;
+    // This block's stream of weight items, all moved by TMA bulk copies into a
+    // ring of A.ring_slots shared-memory slots: first its gate/up units
+    // (u = b + j G: the gate and up rows of one routed neuron), then, per
+    // phase-C output row r = b + j G, the down-projection rows of the active
+    // experts in chunks of A.chunk_experts.  Slots 0..S-1 are filled now; the
+    // warp that consumes item q refills its slot with item q + S, so the
+    // copies of phase C's rows start as soon as phase B frees slots.
+    const int S = A.ring_slots;
+    const int nu = (units > b) ? (units - b + G - 1) / G : 0;
+    const int nr = (s.d > b) ? (s.d - b + G - 1) / G : 0;
+    const int nch = (n_act + A.chunk_experts - 1) / A.chunk_experts;
+    n_items = n_sh + nu + nr * nch;
+    // every slot is free (phase A consumed its items): fill all of them
+    if (warp == 0 && lane < S && n_sh + lane < n_items) {
+      fence_proxy_async_smem();  // after the phase-A reads of the slots, before the copies overwrite them
+      issue_item(A, n_sh + lane, (n_sh + lane) % S, n_sh, nu, nch, b, G, n_act, act_e, ring, full, slot_issued);
     }
-    // gate/up GEMV + SwiGLU; units dealt to blocks first (u = b + j * G)
-    for (int j = warp;; j += kWarps) {
-      const int u = b + j * G;
-      if (u >= units) break;
-      const int a = u / s.I, i = u - a * s.I;
-      const int e = act_e[a];
-      const uint16_t* W = (e < s.E) ? A.gate_up + (size_t)e * 2 * s.I * s.d : A.shared_w;
-      const uint4* grow = reinterpret_cast<const uint4*>(W + (size_t)i * s.d) + lane;
-      const uint4* urow = reinterpret_cast<const uint4*>(W + (size_t)(s.I + i) * s.d) + lane;
-      uint4 gv[NCH], uv[NCH];
-#pragma unroll
-      for (int c = 0; c < NCH; ++c) {
-        gv[c] = __ldcg(grow + 32 * c);
-        uv[c] = __ldcg(urow + 32 * c);
+    // routed gate/up GEMV + SwiGLU: routed unit j (item n_sh + j) goes to warp j mod kWarps
+    for (int j = warp; j < nu; j += kWarps) {
+      const int q = n_sh + j, slot = q % S;
+      if (!wait_item(full, slot_issued, q, S, A.ctl)) {
+        flag_s = 0;
+        break;
       }
+      const int u = b + j * G;
+      const int a = u / s.I, i = u - a * s.I;
+      const uint2* grow = reinterpret_cast<const uint2*>(ring + (size_t)slot * A.slot_bytes) + lane;
+      const uint2* urow = grow + s.d / 4;
       unsigned mm = act_m[a];
       int row = act_row[a];
       while (mm) {
         const int t = __ffs(mm) - 1;
         mm &= mm - 1u;
-        const float* xr = big + (size_t)t * s.d + lane * 8;
+        const float4* xr = reinterpret_cast<const float4*>(big + (size_t)t * s.d) + lane;
         float g = 0.f, up = 0.f;
 #pragma unroll
-        for (int c = 0; c < NCH; ++c) {
-          g += dot8(gv[c], xr + 256 * c);
-          up += dot8(uv[c], xr + 256 * c);
-        }
+        for (int c = 0; c < 2 * NCH; ++c) dot4x2(grow[32 * c], urow[32 * c], xr[32 * c], g, up);
         g = warp_sum(g);
         up = warp_sum(up);
-        if (lane == 0) sc.h_gemv[(size_t)row * s.I + i] = silu(g) * up;
+        if (lane < sc.dec_hreps) st_tagged(dh + (size_t)lane * hrep + (size_t)row * s.I + i, silu(g) * up, ep_s);
         ++row;
+      }
+      __syncwarp();  // every lane has read the slot
+      if (lane == 0 && q + S < n_items) {
+        fence_proxy_async_smem();
+        issue_item(A, q + S, slot, n_sh, nu, nch, b, G, n_act, act_e, ring, full, slot_issued);
       }
     }
   }
-  ok = grid_sync(A.bar, 2, A.ctl, &flag_s) && ok;
+  __syncthreads();  // every warp is done with x in shared memory
+  ok = ok && flag_s != 0;
 
   // ---------------------------------------------------------------- phase C
   if (ok) {
-    const int n_act = n_act_s;
-    const int pairs = s.T * s.k + (s.has_shared ? s.T : 0);
-    constexpr int kBatch = (18 / NCI) > 0 ? (18 / NCI) : 1;  // experts whose rows are loaded together
-    // this warp's first output row: its down rows need nothing from phase B,
-    // so they are requested before h is staged
-    const int r0 = b + warp * G;
-    uint4 wv[kBatch][NCI];
-    if (r0 < s.d) {
+    {
+      // stage this block's copy of h, polling each pair of values until both
+      // carry this launch's tag (the last ones land when the slowest block
+      // finishes phase B)
+      const unsigned long long* src = dh + (size_t)(b % sc.dec_hreps) * hrep;
+      float2* dst = reinterpret_cast<float2*>(big);
+      const int n2 = (int)(hrep >> 1);
+      const unsigned ep = ep_s;
+      const long long t0 = clock64(), lim = wait_cycles(A.ctl);
+      bool late = false;
+      for (int i0 = tid; i0 < n2 && !late; i0 += 8 * kThreads) {
+        unsigned long long lo[8], hi[8];
+        for (int polls = 1;; ++polls) {
+          // the batch is re-read whole until every pair in it is ready, so that
+          // the loads stay independent of each other
 #pragma unroll
-      for (int q = 0; q < kBatch; ++q) {
-        if (q < n_act) {
-          const int e = act_e[q];
-          const uint16_t* Wd = (e < s.E) ? A.down + (size_t)e * s.d * s.I : A.shared_w + (size_t)2 * s.I * s.d;
-          const uint4* row = reinterpret_cast<const uint4*>(Wd + (size_t)r0 * s.I) + lane;
+          for (int u = 0; u < 8; ++u)
+            if (i0 + u * kThreads < n2) ld_tagged2(src + 2 * (i0 + u * kThreads), lo[u], hi[u]);
+          bool ready = true;
 #pragma unroll
-          for (int c = 0; c < NCI; ++c) wv[q][c] = __ldcg(row + 32 * c);
+          for (int u = 0; u < 8; ++u)
+            ready = ready && (i0 + u * kThreads >= n2 || (tag_of(lo[u]) == ep && tag_of(hi[u]) == ep));
+          if (ready) break;
+          if (polls >= 256 && clock64() - t0 > lim) {
+            late = true;
+            break;
+          }
         }
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+          if (i0 + u * kThreads < n2) dst[i0 + u * kThreads] = make_float2(value_of(lo[u]), value_of(hi[u]));
+      }
+      if (late) {
+        raise_status(A.ctl, kStatusTimeout);
+        flag_s = 0;
       }
     }
-    {
-      const float4* src = reinterpret_cast<const float4*>(sc.h_gemv);
-      float4* dst = reinterpret_cast<float4*>(big);
-      const int n4 = (pairs * s.I) >> 2;
-      for (int i = tid; i < n4; i += kThreads) dst[i] = __ldcg(src + i);
-    }
     __syncthreads();
+    ok = flag_s != 0;
+  }
+  if (ok) {
+    const int n_act = n_act_s;
+    const int n_routed = n_act - (s.has_shared ? 1 : 0);
+    const int S = A.ring_slots;
+    const int units = n_routed * s.I;
+    const int nu = (units > b) ? (units - b + G - 1) / G : 0;
+    const int nch = (n_act + A.chunk_experts - 1) / A.chunk_experts;
+    // the next layer's router rows and shared expert, if the caller named them:
+    // pull them into L2 while this phase is bound by latency, not bandwidth
+    // (the last warp: it has no output row when d < kWarps G)
+    if (warp == kWarps - 1) {
+      const size_t rbytes = (size_t)s.E * s.d * 4, sbytes = (size_t)3 * s.I * s.d * 2;
+      const size_t rper = ((rbytes / G) + 4095) & ~size_t(4095), sper = ((sbytes / G) + 4095) & ~size_t(4095);
+      if (A.next_wr)
+        for (size_t off = rper * b + (size_t)lane * 4096; off < min(rbytes, rper * (b + 1)); off += 32 * 4096)
+          prefetch_l2(reinterpret_cast<const uint8_t*>(A.next_wr) + off, (uint32_t)min((size_t)4096, rbytes - off));
+      if (A.next_shared)
+        for (size_t off = sper * b + (size_t)lane * 4096; off < min(sbytes, sper * (b + 1)); off += 32 * 4096)
+          prefetch_l2(reinterpret_cast<const uint8_t*>(A.next_shared) + off,
+                      (uint32_t)min((size_t)4096, sbytes - off));
+    }
     for (int j = warp;; j += kWarps) {
       const int r = b + j * G;
       if (r >= s.d) break;
@@ -385,37 +597,44 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const DecodeA
       float part[MAXT];
 #pragma unroll
       for (int t = 0; t < MAXT; ++t) part[t] = 0.f;
-      for (int a0 = 0; a0 < n_act; a0 += kBatch) {
-        if (j != warp || a0 > 0) {
-#pragma unroll
-          for (int q = 0; q < kBatch; ++q) {
-            if (a0 + q < n_act) {
-              const int e = act_e[a0 + q];
-              const uint16_t* Wd =
-                  (e < s.E) ? A.down + (size_t)e * s.d * s.I : A.shared_w + (size_t)2 * s.I * s.d;
-              const uint4* row = reinterpret_cast<const uint4*>(Wd + (size_t)r * s.I) + lane;
-#pragma unroll
-              for (int c = 0; c < NCI; ++c) wv[q][c] = __ldcg(row + 32 * c);
-            }
-          }
+      bool fail = false;
+      for (int c = 0; c < nch; ++c) {
+        const int q = n_sh + nu + j * nch + c, slot = q % S;
+        if (!wait_item(full, slot_issued, q, S, A.ctl)) {
+          fail = true;
+          break;
         }
+        const int a0 = c * A.chunk_experts;
+        const int na = min(A.chunk_experts, n_act - a0);
+        const uint2* base = reinterpret_cast<const uint2*>(ring + (size_t)slot * A.slot_bytes) + lane;
+        for (int qa = 0; qa < na; ++qa) {
+          const int a = a0 + qa;
+          uint2 wv[2 * NCI];
 #pragma unroll
-        for (int q = 0; q < kBatch; ++q) {
-          if (a0 + q >= n_act) break;
-          const unsigned mm = act_m[a0 + q];
-          const int row0 = act_row[a0 + q];
+          for (int cc = 0; cc < 2 * NCI; ++cc) wv[cc] = base[(size_t)qa * (s.I / 4) + 32 * cc];
+          const unsigned mm = act_m[a];
+          const int row0 = act_row[a];
 #pragma unroll
           for (int t = 0; t < MAXT; ++t) {
             if ((mm >> t) & 1u) {
               const int row = row0 + __popc(mm & ((1u << t) - 1u));
-              const float* hr = big + (size_t)row * s.I + lane * 8;
+              const float4* hr = reinterpret_cast<const float4*>(big + (size_t)row * s.I) + lane;
               float dsum = 0.f;
 #pragma unroll
-              for (int c = 0; c < NCI; ++c) dsum += dot8(wv[q][c], hr + 256 * c);
-              part[t] = fmaf(act_w[a0 + q][t], dsum, part[t]);
+              for (int cc = 0; cc < 2 * NCI; ++cc) dsum = dot4(wv[cc], hr[32 * cc], dsum);
+              part[t] = fmaf(act_w[a][t], dsum, part[t]);
             }
           }
         }
+        __syncwarp();
+        if (lane == 0 && q + S < n_items) {
+          fence_proxy_async_smem();
+          issue_item(A, q + S, slot, n_sh, nu, nch, b, G, n_act, act_e, ring, full, slot_issued);
+        }
+      }
+      if (fail) {
+        flag_s = 0;
+        break;
       }
       float mine = 0.f;
 #pragma unroll
@@ -435,19 +654,23 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const DecodeA
       }
     }
   }
-  // leave: the last block out resets the barrier counters for the next launch
+  // a block that gave up may still have bulk copies in flight into its ring:
+  // wait (bounded) for every issued item before the shared memory is released
+  __syncthreads();
+  if (flag_s == 0 && tid < A.ring_slots) drain_slot(full, slot_issued, tid, A.ctl);
+  // leave: the last block out publishes this launch's epoch (the next launch
+  // tags with epoch + 1) and clears the exit counter
   __syncthreads();
   if (tid == 0) {
     __threadfence();
-    if (atomicAdd(A.bar + 1, 1u) == (unsigned)G - 1) {
+    if (atomicAdd(A.bar, 1u) == (unsigned)G - 1) {
       A.bar[0] = 0u;
-      A.bar[1] = 0u;
+      A.bar[1] = ep_s;
       __threadfence();
     }
   }
 }
 
-size_t decode_smem_bytes(const Shapes& s) { return decode_big_bytes(s); }
 
 template <int NCH, int NCI, int MAXT>
 static const void* pick(bool xbf16) {
@@ -479,9 +702,65 @@ static const void* decode_kernel_for(const Shapes& s) {
   return nullptr;
 }
 
+// Dynamic shared memory a kernel instantiation may use: the per-block opt-in
+// maximum less its static shared memory (looked up once per kernel and device).
+static int decode_dyn_limit(const void* k) {
+  struct Entry {
+    const void* k;
+    int dev, lim;
+  };
+  static Entry cache[128];
+  static int n_cache = 0;
+  static std::mutex mu;
+  int dev = 0;
+  if (!k || cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  std::lock_guard<std::mutex> lock(mu);
+  for (int i = 0; i < n_cache; ++i)
+    if (cache[i].k == k && cache[i].dev == dev) return cache[i].lim;
+  int optin = 0;
+  cudaFuncAttributes fa;
+  if (cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess ||
+      cudaFuncGetAttributes(&fa, k) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  const int lim = optin - (int)fa.sharedSizeBytes;
+  if (n_cache < 128) cache[n_cache++] = {k, dev, lim};
+  return lim;
+}
+
+// The weight ring: slots hold one gate/up unit (2 d bf16) or the down rows of
+// top_k + 1 experts (a whole phase-C row at batch 1), whichever is larger; as
+// many slots as the shared memory left after x / h holds, up to kMaxSlots.
+struct DecodeRing {
+  int slots, slot_bytes, chunk;
+};
+static DecodeRing decode_ring(const Shapes& s, int max_smem) {
+  DecodeRing r{0, 0, 0};
+  const void* k = decode_kernel_for(s);
+  if (!k) return r;
+  const int lim = decode_dyn_limit(k);
+  const long long budget = (long long)(max_smem < lim ? max_smem : lim) - (long long)decode_big_bytes(s);
+  const int unit = 4 * s.d, drow = 2 * s.I * (s.k + 1);
+  r.slot_bytes = unit > drow ? unit : drow;
+  r.chunk = r.slot_bytes / (2 * s.I);
+  const long long n = budget > 0 ? budget / r.slot_bytes : 0;
+  r.slots = (int)(n < kMaxSlots ? n : kMaxSlots);
+  return r;
+}
+
+size_t decode_smem_bytes(const Shapes& s, int max_smem) {
+  const DecodeRing r = decode_ring(s, max_smem);
+  return decode_big_bytes(s) + (size_t)r.slots * r.slot_bytes;
+}
+
 bool decode_supported(const Shapes& s, int max_smem) {
-  return s.T <= 16 && s.d % 256 == 0 && s.I % 256 == 0 && decode_kernel_for(s) != nullptr &&
-         decode_smem_bytes(s) <= (size_t)max_smem;
+  const void* k = decode_kernel_for(s);
+  if (!(s.T <= 16 && s.d % 256 == 0 && s.I % 256 == 0 && k != nullptr)) return false;
+  return decode_ring(s, max_smem).slots >= 2;
 }
 
 cudaError_t prepare_decode_kernels(int max_smem) {
@@ -496,24 +775,35 @@ cudaError_t prepare_decode_kernels(int max_smem) {
           s.x_bf16 = xb;
           const void* k = decode_kernel_for(s);
           if (!k) continue;
-          cudaError_t err = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
+          const int lim = decode_dyn_limit(k);
+          cudaError_t err =
+              cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem < lim ? max_smem : lim);
           if (err != cudaSuccess) return err;
         }
   return cudaSuccess;
 }
 
-int decode_blocks_per_sm(const Shapes& s) {
+int decode_blocks_per_sm(const Shapes& s, int max_smem) {
   int n = 0;
   const void* k = decode_kernel_for(s);
-  if (!k || cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k, kThreads, decode_smem_bytes(s)) != cudaSuccess)
+  if (!k ||
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k, kThreads, decode_smem_bytes(s, max_smem)) != cudaSuccess)
     return 0;
   return n;
 }
 
 cudaError_t launch_decode_fused(const Shapes& s, const void* x, const float* wr, const float* rb,
                                 const uint16_t* gate_up, const uint16_t* down, const uint16_t* shared_w, void* y,
-                                const Scratch& sc, const DevCtl& ctl, unsigned* bar, int num_sms, cudaStream_t st) {
+                                const Scratch& sc, const DevCtl& ctl, unsigned* bar, int num_sms, cudaStream_t st,
+                                const float* next_wr, const uint16_t* next_shared, int max_smem) {
+  const DecodeRing ring = decode_ring(s, max_smem);
+  if (ring.slots < 2) return cudaErrorInvalidValue;
   DecodeArgs a;
+  a.ring_slots = ring.slots;
+  a.slot_bytes = ring.slot_bytes;
+  a.chunk_experts = ring.chunk;
+  a.next_wr = next_wr;
+  a.next_shared = next_shared;
   a.s = s;
   a.x = x;
   a.wr = wr;
@@ -531,7 +821,7 @@ cudaError_t launch_decode_fused(const Shapes& s, const void* x, const float* wr,
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(num_sms);
   cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = decode_smem_bytes(s);
+  cfg.dynamicSmemBytes = decode_big_bytes(s) + (size_t)ring.slots * ring.slot_bytes;
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeCooperative;
@@ -557,7 +847,6 @@ cudaError_t launch_decode_fused(const Shapes& s, const void* x, const float* wr,
 // cudaGetSymbolAddress; the array's name in host code is only a host-side
 // stand-in, never a device address.
 // ---------------------------------------------------------------------------
-#include <mutex>
 
 using namespace moe;
 
@@ -566,14 +855,17 @@ namespace {
 constexpr int kNoAllocMaxT = 16;
 constexpr int kNoAllocMaxTopK = 8;
 constexpr int kNoAllocMaxInter = 1024;
-constexpr size_t kNoAllocH = (size_t)kNoAllocMaxT * (kNoAllocMaxTopK + 1) * kNoAllocMaxInter * 4;  // fp32 h rows
-constexpr size_t kNoAllocLogits = (size_t)kNoAllocMaxT * kMaxExperts * 4;
+constexpr size_t kNoAllocH = (size_t)kNoAllocMaxT * (kNoAllocMaxTopK + 1) * kNoAllocMaxInter * 8;  // tagged h rows
+constexpr int kNoAllocReps = 4;  // copies of the logits
+constexpr size_t kNoAllocLogits = (size_t)kNoAllocReps * kNoAllocMaxT * kMaxExperts * 8;  // tagged logits
 constexpr size_t kNoAllocPicks = (size_t)kNoAllocMaxT * kNoAllocMaxTopK * 4;
 constexpr size_t kNoAllocOffLogits = kNoAllocH;
 constexpr size_t kNoAllocOffIdx = kNoAllocOffLogits + kNoAllocLogits;
 constexpr size_t kNoAllocOffW = kNoAllocOffIdx + kNoAllocPicks;
-constexpr size_t kNoAllocOffWords = kNoAllocOffW + kNoAllocPicks;  // [0] status, [2..3] barrier counters
-constexpr size_t kNoAllocBytes = kNoAllocOffWords + 256;
+constexpr size_t kNoAllocOffStatus = kNoAllocOffW + kNoAllocPicks;
+constexpr size_t kNoAllocOffBar = kNoAllocOffStatus + 256;  // exit counter and epoch
+constexpr size_t kNoAllocBarBytes = 256;
+constexpr size_t kNoAllocBytes = kNoAllocOffBar + kNoAllocBarBytes;
 
 struct NoAllocDevice {
   bool ready = false;
@@ -586,9 +878,11 @@ std::mutex g_noalloc_mu;
 
 }  // namespace
 
-// The scratch array (about 600 KB).  Every call shares it and it keeps the
-// last call's contents; the barrier counters, which must start at zero, are
-// cleared at the start of every call.
+// The scratch array (about 1.3 MB).  Every call shares it and it keeps the
+// last call's contents.  Its zero initial contents are a valid start: tag 0
+// is never a launch's epoch.  The exit counter, which must be zero when a
+// launch starts, is cleared at the start of every call; the epoch word is
+// kept, since a tag left by an earlier call must never match a later one.
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocBytes];
 
 extern "C" int moe_decode_noalloc(const void* x, int T, int x_dtype, int d, int n_experts, int inter, int top_k,
@@ -614,7 +908,7 @@ extern "C" int moe_decode_noalloc(const void* x, int T, int x_dtype, int d, int 
   s.k = top_k;
   s.has_shared = shared_w != nullptr;
   s.x_bf16 = x_dtype == MOE_BF16;
-  const int smem_limit = 200 * 1024;
+  const int smem_limit = kDecodeSmemLimit;
   if (!decode_supported(s, smem_limit)) return MOE_ERR_UNSUPPORTED;
 
   // set-up, once per device, with that device current
@@ -643,15 +937,17 @@ extern "C" int moe_decode_noalloc(const void* x, int T, int x_dtype, int d, int 
     }
     nd = slot;
   }
-  if (decode_blocks_per_sm(s) < 1) return MOE_ERR_UNSUPPORTED;
+  if (decode_blocks_per_sm(s, smem_limit) < 1) return MOE_ERR_UNSUPPORTED;
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  unsigned* words = reinterpret_cast<unsigned*>(nd.base + kNoAllocOffWords);
-  unsigned* bar = words + 2;
-  if (cudaMemsetAsync(bar, 0, 2 * sizeof(unsigned), st) != cudaSuccess) return MOE_ERR_CUDA;
+  unsigned* words = reinterpret_cast<unsigned*>(nd.base + kNoAllocOffStatus);
+  unsigned* bar = reinterpret_cast<unsigned*>(nd.base + kNoAllocOffBar);
+  if (cudaMemsetAsync(bar, 0, sizeof(unsigned), st) != cudaSuccess) return MOE_ERR_CUDA;
   Scratch sc{};
-  sc.h_gemv = reinterpret_cast<float*>(nd.base);
-  sc.logits = reinterpret_cast<float*>(nd.base + kNoAllocOffLogits);
+  sc.dec_h = reinterpret_cast<float*>(nd.base);
+  sc.dec_hreps = 1;
+  sc.dec_logits = reinterpret_cast<float*>(nd.base + kNoAllocOffLogits);
+  sc.dec_reps = kNoAllocReps;
   sc.idx = reinterpret_cast<int*>(nd.base + kNoAllocOffIdx);
   sc.w = reinterpret_cast<float*>(nd.base + kNoAllocOffW);
   sc.status = status ? status : words;
@@ -663,6 +959,6 @@ extern "C" int moe_decode_noalloc(const void* x, int T, int x_dtype, int d, int 
   const cudaError_t err =
       launch_decode_fused(s, x, router_w, router_b, static_cast<const uint16_t*>(experts_gate_up),
                           static_cast<const uint16_t*>(experts_down), static_cast<const uint16_t*>(shared_w), y, sc,
-                          ctl, bar, nd.sms, st);
+                          ctl, bar, nd.sms, st, nullptr, nullptr, smem_limit);
   return err == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }

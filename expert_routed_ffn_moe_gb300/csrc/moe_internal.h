@@ -44,7 +44,11 @@ struct Scratch {
   float* h_gemv;          // [Tg*k + Tg, I] fp32 SwiGLU activations (GEMV path)
   uint16_t* out;          // [T*k + T, d] bf16 expert outputs, grouped rows (GEMM path)
   unsigned* status;       // device status word
-  unsigned* gridbar;      // [2] arrival / departure counters of the fused decode kernel's grid barriers
+  unsigned* gridbar;      // fused decode kernel: [0] exit counter, [1] epoch of the last launch
+  float* dec_logits;      // fused decode kernel: [dec_reps][T][E] router logits as (fp32, epoch) 64-bit words
+  float* dec_h;           // fused decode kernel: [dec_hreps][T*k + T][I] SwiGLU activations as (fp32, epoch) words
+  int dec_reps;           // copies of the logits (blocks read copy b % reps)
+  int dec_hreps;          // copies of h
   int max_mtiles;
 };
 
@@ -93,13 +97,17 @@ cudaError_t launch_gemm_router(const Shapes& s, const GemmMaps& m, const Scratch
                                int num_sms, cudaStream_t st);
 
 // moe_decode.cu
-size_t decode_smem_bytes(const Shapes& s);
+// Shared memory the fused decode kernel may use (clamped to what the device
+// allows a block next to the kernel's static shared memory).
+constexpr int kDecodeSmemLimit = 227 * 1024;
+size_t decode_smem_bytes(const Shapes& s, int max_smem);
 bool decode_supported(const Shapes& s, int max_smem);
-int decode_blocks_per_sm(const Shapes& s);
+int decode_blocks_per_sm(const Shapes& s, int max_smem);
 cudaError_t prepare_decode_kernels(int max_smem);
 cudaError_t launch_decode_fused(const Shapes& s, const void* x, const float* wr, const float* rb,
                                 const uint16_t* gate_up, const uint16_t* down, const uint16_t* shared_w, void* y,
-                                const Scratch& sc, const DevCtl& ctl, unsigned* bar, int num_sms, cudaStream_t st);
+                                const Scratch& sc, const DevCtl& ctl, unsigned* bar, int num_sms, cudaStream_t st,
+                                const float* next_wr, const uint16_t* next_shared, int max_smem);
 
 // moe_combine.cu
 cudaError_t launch_permute_rows(const Shapes& s, const void* x, const Scratch& sc, const DevCtl& ctl,

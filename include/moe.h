@@ -64,7 +64,8 @@ extern "C" {
 #define MOE_PATH_AUTO 0        /* small T: GEMV over the selected experts; otherwise grouped GEMM */
 #define MOE_PATH_GEMV 1        /* bandwidth-bound GEMV over the selected experts (small T only, else
                                   MOE_ERR_UNSUPPORTED); for T <= 16 when shapes allow, the whole layer
-                                  runs as one cooperative kernel with two grid barriers */
+                                  runs as one cooperative kernel whose blocks wait on each other's
+                                  published logits and activations (epoch-tagged words) */
 #define MOE_PATH_GEMM 2        /* tcgen05/TMEM grouped GEMM */
 
 /* router logit kernel (moe_set_router) */
@@ -128,6 +129,15 @@ int moe_set_path(moe_ctx* ctx, int path);
  * unknown value. */
 int moe_set_router(moe_ctx* ctx, int router);
 
+/* Prefetch hint for stacked layers: the next moe_forward call on `ctx` that
+ * takes the small-T path pulls `next_router_w` ([E, d] fp32) and
+ * `next_shared_w` (shared gate_up + down, bf16) -- the weights the following
+ * layer reads first -- into L2 while its own last phase is bound by latency,
+ * so that the following layer starts from L2.  Either may be NULL.  The hint
+ * serves one call, then clears.  It only moves data into the cache; results
+ * do not depend on it.  MOE_ERR_ALIGN if a pointer is not 16-byte aligned. */
+int moe_set_prefetch(moe_ctx* ctx, const float* next_router_w, const void* next_shared_w);
+
 /* Synchronise the device, then read and clear the context's device status
  * word: MOE_OK, or the first MOE_ERR_TIMEOUT / MOE_ERR_BOUNDS latched by a
  * kernel since the last call; MOE_ERR_CUDA if the synchronisation itself
@@ -135,7 +145,7 @@ int moe_set_router(moe_ctx* ctx, int router);
 int moe_status(moe_ctx* ctx);
 
 /* Bounded waits: how long (nanoseconds, measured in SM clock cycles at 2 per
- * ns) a kernel polls a barrier before giving up with MOE_ERR_TIMEOUT.  A wait
+ * ns) a kernel polls a barrier or a published value before giving up with MOE_ERR_TIMEOUT.  A wait
  * always polls at least 256 times before it looks at the clock.  0 restores
  * the default (1 s).  MOE_ERR_ARG if negative. */
 int moe_set_spin_limit(moe_ctx* ctx, long long limit);
@@ -160,12 +170,18 @@ int moe_set_spin_limit(moe_ctx* ctx, long long limit);
  * events are not recorded.  MOE_ERR_ARG on a bad id or null event. */
 int moe_time_kernel(moe_ctx* ctx, int kernel_id, void* ev_start, void* ev_stop);
 
+/* Record the CUDA event `event` (a cudaEvent_t created with timing) on
+ * `stream`; under stream capture the record becomes a timeable event node of
+ * the graph (plain cudaEventRecord there only orders streams).  Profiling
+ * helper for timing a run of launches.  MOE_ERR_ARG on a null event. */
+int moe_record_event(void* event, void* stream);
+
 /* Number of kernels this context has launched (or captured) so far. */
 long long moe_launch_count(moe_ctx* ctx);
 
 /* Test hook for failure detection without a GPU fault: with on = 1, later
  * calls make the grouped GEMM's MMA thread, and every block of the fused
- * decode kernel at its first grid barrier, wait once for an event that never
+ * decode kernel where it waits for the router logits, wait once for an event that never
  * happens.  The bounded wait runs out after the spin limit, the kernel records
  * MOE_ERR_TIMEOUT, drains its in-flight copies, frees its tensor memory and
  * returns; moe_status then reports the timeout.  on = 0 turns it off.
@@ -196,8 +212,8 @@ int moe_inject_stall(moe_ctx* ctx, int on);
  * anything is launched.  The first call on each device looks up the array's
  * device address (cudaGetSymbolAddress) and sets kernel attributes, with that
  * device current: make that first call before any stream capture.  Every call
- * shares the one array, which keeps the previous call's contents (the barrier
- * counters that must start at zero are cleared by each call on `stream`), so
+ * shares the one array, which keeps the previous call's contents (the exit
+ * counter that must start at zero is cleared by each call on `stream`), so
  * calls that overlap on the GPU -- on different streams, or from different
  * threads -- race and must not be issued.  Asynchronous on `stream`. */
 int moe_decode_noalloc(const void* x, int T, int x_dtype, int d, int n_experts, int inter, int top_k,

@@ -207,10 +207,10 @@ def test_modular_gemv_path_beyond_fused_limit():
 
 
 def test_fused_decode_barrier_timeout_and_recovery():
-    # The injected stall makes every block wait at the first grid barrier for
-    # one arrival more than there are blocks; with a 1 ms limit the wait runs
-    # out, the status word reports it, moe_status resets the barrier counters,
-    # and the next call on the same context is correct.
+    # The injected stall makes every block wait for router logits tagged with
+    # an epoch that no block writes; with a 1 ms limit the wait runs out, the
+    # status word reports it, and the next call on the same context (a new
+    # epoch) is correct and does not take the failed call's values as ready.
     w = W["decode"]
     inp = layer_inputs(w, 2)
     layer = make_layer(w)
