@@ -34,9 +34,11 @@
 // polls the words it needs until all carry the current epoch (bounded spin,
 // MOE_ERR_TIMEOUT).  Data and readiness travel in one access, so a block
 // starts on the logits one L2 round trip after the last of them lands, instead
-// of after a barrier's arrive, poll and release and then a separate load.  The
-// last block to leave publishes the launch's epoch; the next launch, a graph
-// replay included, tags with the one after it.
+// of after a barrier's arrive, poll and release and then a separate load.
+// (Per-block "h written" flags behind a fence measured slower: the fence waits
+// out the block's in-flight traffic.)  The last block to leave publishes the
+// launch's epoch; the next launch, a graph replay included, tags with the one
+// after it.
 #include <math.h>
 
 #include <mutex>
@@ -51,7 +53,11 @@ constexpr int kWarps = 16;
 constexpr int kRowChunks = 4;                    // warps sharing one router row
 constexpr int kSlots = kWarps / kRowChunks;      // router rows per pass
 constexpr int kThreads = kWarps * 32;
-constexpr int kMaxSlots = 32;                    // TMA ring slots (upper bound)
+constexpr int kMaxSlots = 32;                    // TMA ring slots (array bound)
+// Ring depth used: measured at batch 1 (d = 2048, 9 active experts), 14 slots
+// of 9 KB beat both 12 (too little in flight) and 16..22 (more bytes queued per
+// SM only spread the blocks' finishing times further apart).
+constexpr int kRingSlots = 14;
 
 MOE_DEV void prefetch_l2(const void* p, uint32_t bytes) {
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(p)), "r"(bytes)
@@ -748,7 +754,7 @@ static DecodeRing decode_ring(const Shapes& s, int max_smem) {
   r.slot_bytes = unit > drow ? unit : drow;
   r.chunk = r.slot_bytes / (2 * s.I);
   const long long n = budget > 0 ? budget / r.slot_bytes : 0;
-  r.slots = (int)(n < kMaxSlots ? n : kMaxSlots);
+  r.slots = (int)(n < kRingSlots ? n : kRingSlots);
   return r;
 }
 
