@@ -270,6 +270,10 @@ def run_ours(args, rank, world, dev):
     dom = dominant_kernel(eff_path)
 
     whole_layer = eff_path == moe.MOE_PATH_GEMV  # the dominant kernel is the whole layer
+    if layers > 1:
+        # stacked layers with fixed weights: a layer's blocks may start on its
+        # weights while the previous layer's kernel finishes (moe_set_overlap)
+        moe.moe_set_overlap(ctx.ctx, True)
 
     def step(ev_pair=None, e2e=False):
         if ev_pair is not None and whole_layer:

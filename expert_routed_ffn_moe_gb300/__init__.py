@@ -55,6 +55,8 @@ def lib() -> ctypes.CDLL:
         L.moe_set_spin_limit.argtypes = [P, ctypes.c_longlong]
         L.moe_record_event.argtypes = [P, P]
         L.moe_record_event.restype = I
+        L.moe_set_overlap.argtypes = [P, I]
+        L.moe_set_overlap.restype = I
         L.moe_set_prefetch.argtypes = [P, P, P]
         L.moe_set_prefetch.restype = I
         L.moe_inject_stall.argtypes = [P, I]
@@ -142,6 +144,12 @@ def moe_set_spin_limit(ctx, limit_ns: int) -> None:
 def moe_record_event(event, stream=None) -> None:
     """Record a torch.cuda.Event on a stream; timeable also under graph capture."""
     _check(lib().moe_record_event(ctypes.c_void_p(event.cuda_event), _stream(stream)), "moe_record_event")
+
+
+def moe_set_overlap(ctx, on: bool) -> None:
+    """Launch the fused small-T kernel with programmatic stream serialization
+    (see moe.h); the caller promises the preceding work does not write the weights."""
+    _check(lib().moe_set_overlap(ctx, 1 if on else 0), "moe_set_overlap")
 
 
 def moe_set_prefetch(ctx, next_router_w=None, next_shared_w=None) -> None:

@@ -24,6 +24,7 @@ struct moe_ctx {
   long long spin_ns = 0;
   int stall = 0;            // test hook (moe_inject_stall)
   const float* next_wr = nullptr;         // prefetch hint for the next call (moe_set_prefetch)
+  bool overlap = false;                   // programmatic launch overlap (moe_set_overlap)
   const uint16_t* next_shared = nullptr;
   int gemv_max_t = 0;       // largest T the GEMV kernels accept for this shape (0: none)
   int decode_max_t = 0;     // largest T the fused decode kernel accepts (0: none)
@@ -335,6 +336,12 @@ int moe_record_event(void* event, void* stream) {
   return cuda_fail(record_event(static_cast<cudaEvent_t>(event), static_cast<cudaStream_t>(stream)));
 }
 
+int moe_set_overlap(moe_ctx* ctx, int on) {
+  if (!ctx || (on != 0 && on != 1)) return MOE_ERR_ARG;
+  ctx->overlap = on == 1;
+  return MOE_OK;
+}
+
 int moe_set_prefetch(moe_ctx* ctx, const float* next_router_w, const void* next_shared_w) {
   if (!ctx) return MOE_ERR_ARG;
   if ((next_router_w && !aligned16(next_router_w)) || (next_shared_w && !aligned16(next_shared_w)))
@@ -408,7 +415,7 @@ int moe_forward(moe_ctx* ctx, const void* x, int T, const float* router_w, const
     // the whole layer in one cooperative launch
     const cudaError_t err = launch(ctx, MOE_K_DECODE_FUSED, st, [&] {
       return launch_decode_fused(s, x, router_w, router_b, gu, dn, sw, y, ctx->sc, ctl, ctx->sc.gridbar,
-                                 ctx->num_sms, st, ctx->next_wr, ctx->next_shared, kDecodeSmemLimit);
+                                 ctx->num_sms, st, ctx->next_wr, ctx->next_shared, kDecodeSmemLimit, ctx->overlap);
     });
     ctx->next_wr = nullptr;  // a hint serves one call
     ctx->next_shared = nullptr;

@@ -256,8 +256,6 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const DecodeA
   const int n_sh = s.has_shared ? ((s.I > b) ? (s.I - b + G - 1) / G : 0) : 0;  // shared-expert units
 
   if (tid == 0) {
-    const unsigned e = ld_relaxed(A.bar + 1) + 1u;  // the previous launch's epoch + 1 (0 is never a tag)
-    ep_s = e ? e : 1u;
     flag_s = 1;
     for (int i = 0; i < A.ring_slots; ++i) {
       mbar_init(&full[i], 1);
@@ -292,6 +290,15 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const DecodeA
     if (tid == 0)
       for (int q = 0; q < n_sh && q < A.ring_slots; ++q)
         issue_item(A, q, q, n_sh, 0, 1, b, G, 0, nullptr, ring, full, slot_issued);
+    // Everything above reads weights only.  Launched with programmatic stream
+    // serialization, this block may have started while the previous kernel
+    // on the stream is still running: wait for it before touching x or any
+    // scratch (a no-op for a normal launch).
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    if (tid == 0) {
+      const unsigned e = ld_relaxed(A.bar + 1) + 1u;  // the previous launch's epoch + 1 (0 is never a tag)
+      ep_s = e ? e : 1u;
+    }
     const int nx = s.T * s.d;
     if (XBF16) {
       const uint32_t* xb = static_cast<const uint32_t*>(A.x);
@@ -534,6 +541,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const DecodeA
   ok = ok && flag_s != 0;
 
   // ---------------------------------------------------------------- phase C
+  // a dependent launch (the next layer) may be scheduled now; its blocks take
+  // an SM as ours leave
+  asm volatile("griddepcontrol.launch_dependents;");
   if (ok) {
     {
       // stage this block's copy of h, polling each pair of values until both
@@ -801,7 +811,7 @@ int decode_blocks_per_sm(const Shapes& s, int max_smem) {
 cudaError_t launch_decode_fused(const Shapes& s, const void* x, const float* wr, const float* rb,
                                 const uint16_t* gate_up, const uint16_t* down, const uint16_t* shared_w, void* y,
                                 const Scratch& sc, const DevCtl& ctl, unsigned* bar, int num_sms, cudaStream_t st,
-                                const float* next_wr, const uint16_t* next_shared, int max_smem) {
+                                const float* next_wr, const uint16_t* next_shared, int max_smem, bool overlap) {
   const DecodeRing ring = decode_ring(s, max_smem);
   if (ring.slots < 2) return cudaErrorInvalidValue;
   DecodeArgs a;
@@ -829,11 +839,13 @@ cudaError_t launch_decode_fused(const Shapes& s, const void* x, const float* wr,
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = decode_big_bytes(s) + (size_t)ring.slots * ring.slot_bytes;
   cfg.stream = st;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeCooperative;
   attr[0].val.cooperative = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = overlap ? 2 : 1;
   return cudaLaunchKernelExC(&cfg, k, params);
 }
 

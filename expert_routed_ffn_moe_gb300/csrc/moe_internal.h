@@ -107,7 +107,8 @@ cudaError_t prepare_decode_kernels(int max_smem);
 cudaError_t launch_decode_fused(const Shapes& s, const void* x, const float* wr, const float* rb,
                                 const uint16_t* gate_up, const uint16_t* down, const uint16_t* shared_w, void* y,
                                 const Scratch& sc, const DevCtl& ctl, unsigned* bar, int num_sms, cudaStream_t st,
-                                const float* next_wr, const uint16_t* next_shared, int max_smem);
+                                const float* next_wr, const uint16_t* next_shared, int max_smem,
+                                bool overlap = false);
 
 // moe_combine.cu
 cudaError_t launch_permute_rows(const Shapes& s, const void* x, const Scratch& sc, const DevCtl& ctl,

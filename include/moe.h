@@ -138,6 +138,17 @@ int moe_set_router(moe_ctx* ctx, int router);
  * do not depend on it.  MOE_ERR_ALIGN if a pointer is not 16-byte aligned. */
 int moe_set_prefetch(moe_ctx* ctx, const float* next_router_w, const void* next_shared_w);
 
+/* Launch overlap for back-to-back layers (no counterpart in the source pages;
+ * a CUDA launch option).  With on = 1, later moe_forward calls that take the
+ * fused small-T kernel launch it with programmatic stream serialization: its
+ * blocks may start while the preceding kernel on the stream is finishing, and
+ * read only the weights (router_w, shared_w) before they wait for that kernel
+ * to complete; x, y and all scratch are touched after the wait.  The caller
+ * promises that the work preceding each such call on its stream does not
+ * write those weight arrays.  on = 0 (the default) launches normally.
+ * MOE_ERR_ARG on other values. */
+int moe_set_overlap(moe_ctx* ctx, int on);
+
 /* Synchronise the device, then read and clear the context's device status
  * word: MOE_OK, or the first MOE_ERR_TIMEOUT / MOE_ERR_BOUNDS latched by a
  * kernel since the last call; MOE_ERR_CUDA if the synchronisation itself

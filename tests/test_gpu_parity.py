@@ -229,3 +229,41 @@ def test_fused_decode_barrier_timeout_and_recovery():
     layer.close()
     assert torch.equal(y, y2)
     check_y(y_host(y), oracle_y(w, inp, [0]), "after barrier timeout")
+
+
+def test_overlapped_decode_launches_match_plain():
+    # Programmatic launch overlap lets a layer's blocks start while the
+    # previous layer's kernel finishes; they must read x (the previous
+    # layer's output) only after waiting for it.  Chain three layers through
+    # x -> y -> x on one stream, with and without overlap, eagerly and from a
+    # CUDA graph: all four results must be bitwise equal.
+    w = W["decode"]
+    inps = [layer_inputs(w, i) for i in range(3)]
+    devs = [device_inputs(w, inp) for inp in inps]
+    layer = make_layer(w)
+    st = torch.cuda.Stream()
+
+    def chain():
+        x = devs[0]["x"]
+        for d in devs:
+            y = torch.empty_like(x)
+            moe.moe_forward(layer.ctx, x, d["router_w"], d["router_b"], d["gate_up"], d["down"], d["shared"],
+                            w.k, y, st)
+            x = y
+        return x
+
+    outs = []
+    for on in (False, True):
+        moe.moe_set_overlap(layer.ctx, on)
+        with torch.cuda.stream(st):
+            outs.append(chain().clone())
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=st):
+                yg = chain()
+            g.replay()
+        st.synchronize()
+        outs.append(yg.clone())
+    assert layer.status() == moe.MOE_OK
+    layer.close()
+    for o in outs[1:]:
+        assert torch.equal(o, outs[0])
