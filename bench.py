@@ -30,8 +30,11 @@ a bounded sample of the same workload on the host cores.
 from __future__ import annotations
 
 import argparse
+import glob
+import hashlib
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -48,6 +51,35 @@ import moe_workloads as mw  # noqa: E402
 
 METRIC = "MoE-layer tokens/s (decode T=1, prefill T=4096) on 1 GB300; % HBM / bf16 roofline"
 UNIT = "tokens/s"
+L2_BYTES = 126 * 1024 * 1024  # GB300 L2 (cudaDeviceProp.l2CacheSize)
+HERE = os.path.dirname(os.path.abspath(__file__))
+CSRC = os.path.join(HERE, "expert_routed_ffn_moe_gb300", "csrc")
+# sources that decide each dominant kernel's code (its traffic record is void once they change)
+KERNEL_SOURCES = {
+    "decode_fused_kernel": ["moe_decode.cu", "moe_common.cuh", "moe_internal.h"],
+    "grouped_gemm_kernel<gate_up>": ["moe_gemm.cu", "moe_common.cuh", "moe_internal.h"],
+}
+
+
+def kernel_source_hash(kernel):
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES[kernel]:
+        with open(os.path.join(CSRC, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(kernel):
+    """DRAM bytes per launch (read + write) of `kernel` from the ncu summaries under
+    profiles/, if one was taken of the current source; else None."""
+    want = kernel_source_hash(kernel)
+    for path in sorted(glob.glob(os.path.join(HERE, "profiles", "*.md"))):
+        with open(path) as fh:
+            for line in fh:
+                m = re.match(r"traffic-record: kernel=(\S+) source_sha256=(\w+) bytes_per_launch=(\d+)", line.strip())
+                if m and m.group(1) == kernel and m.group(2) == want:
+                    return int(m.group(3))
+    return None
 GRAPH_STEPS = 50  # steps per captured graph; longer runs replay it
 EVENT_EVERY = 5   # steps between two event-timed launches of the dominant kernel
 
@@ -251,7 +283,7 @@ def run_ours(args, rank, world, dev):
 
     moe.build()
     w = mw.WORKLOADS[args.workload]
-    layers = w.layers
+    layers = args.layers or w.layers
     peaks = load_peaks()
     torch.cuda.set_device(dev)
     stream = torch.cuda.Stream(device=dev)
@@ -383,7 +415,7 @@ def run_ours(args, rank, world, dev):
         per_launch = statistics.mean(c["layer_bytes"] for c in costs)
         achieved = per_launch / (kern_avg_ms / 1e3) / 1e9
         roof = dict(bound="hbm", achieved=round(achieved, 1), peak=peaks["hbm_gbs"], unit="GB/s",
-                    frac=round(achieved / peaks["hbm_gbs"], 4), traffic=None,
+                    frac=round(achieved / peaks["hbm_gbs"], 4), traffic=profiled_traffic("decode_fused_kernel"),
                     kernel="decode_fused_kernel (whole layer)", algorithmic_bytes_per_launch=int(per_launch),
                     avg_launch_us=round(kern_avg_ms * 1e3, 2), peak_source=peaks["source"])
     else:
@@ -398,6 +430,7 @@ def run_ours(args, rank, world, dev):
         else:
             roof = dict(bound="tensor", achieved=round(tfs, 1), peak=peaks["bf16_tflops"], unit="TFLOP/s",
                         frac=round(tc_frac, 4), traffic=None)
+        roof["traffic"] = profiled_traffic("grouped_gemm_kernel<gate_up>")
         roof.update(kernel="grouped_gemm_kernel<gate_up>", algorithmic_bytes_per_launch=int(per_launch_b),
                     algorithmic_flops_per_launch=int(per_launch_f), avg_launch_us=round(kern_avg_ms * 1e3, 2),
                     tensor_frac=round(tc_frac, 4), hbm_frac=round(hbm_frac, 4), peak_source=peaks["source"])
@@ -425,7 +458,11 @@ def run_ours(args, rank, world, dev):
                    config=dict(workload=w.name, tokens_per_layer=w.T, layers_per_step=layers, d=w.d, experts=w.E,
                                inter=w.I, shared_inter=w.I_s, top_k=w.k,
                                path="gemv" if eff_path == moe.MOE_PATH_GEMV else "grouped_gemm",
-                               l2="inputs larger than L2 (distinct weights per layer, >126 MB per step)",
+                               l2=(f"inputs larger than L2 (distinct weights per layer, "
+                                   f"{layer_bytes * layers / 1e6:.0f} MB touched per step)"
+                                   if layer_bytes * layers > L2_BYTES else
+                                   f"inputs fit in L2 ({layer_bytes * layers / 1e6:.0f} MB per step): "
+                                   f"a profiling run, not a bench number"),
                                parallelism=f"replicas x{world}"),
                    e2e=dict(value=round(e2e_value, 1), unit=UNIT,
                             h2d_bytes_per_step=int(sum(t.numel() * t.element_size() for t in xh)),
@@ -480,6 +517,8 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--ref-step-seconds", type=float, default=3.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--layers", type=int, default=0,
+                    help="stacked layers per step (default: the workload's own; fewer only for small profiling runs)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
