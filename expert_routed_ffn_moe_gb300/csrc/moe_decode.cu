@@ -623,7 +623,33 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const DecodeA
         const int a0 = c * A.chunk_experts;
         const int na = min(A.chunk_experts, n_act - a0);
         const uint2* base = reinterpret_cast<const uint2*>(ring + (size_t)slot * A.slot_bytes) + lane;
-        for (int qa = 0; qa < na; ++qa) {
+        if (MAXT == 1) {
+          // batch 1 (one token per expert, h row act_row[a]): three experts per
+          // step with independent partial sums, so the shared-memory loads and
+          // FMA chains of different experts overlap (one expert at a time, the
+          // loop was latency-bound: ~430 cycles per expert)
+          float ps[3] = {0.f, 0.f, 0.f};
+          for (int qa0 = 0; qa0 < na; qa0 += 3) {
+#pragma unroll
+            for (int u = 0; u < 3; ++u) {
+              const int qa = qa0 + u;
+              if (qa < na) {
+                const int a = a0 + qa;
+                const float4* hr = reinterpret_cast<const float4*>(big + (size_t)act_row[a] * s.I) + lane;
+                const uint2* wr = base + (size_t)qa * (s.I / 4);
+                float d0 = 0.f, d1 = 0.f;
+#pragma unroll
+                for (int cc = 0; cc < 2 * NCI; cc += 2) {
+                  d0 = dot4(wr[32 * cc], hr[32 * cc], d0);
+                  d1 = dot4(wr[32 * (cc + 1)], hr[32 * (cc + 1)], d1);
+                }
+                ps[u] = fmaf(act_w[a][0], d0 + d1, ps[u]);
+              }
+            }
+          }
+          part[0] += (ps[0] + ps[1]) + ps[2];
+        }
+        for (int qa = 0; qa < na && MAXT > 1; ++qa) {
           const int a = a0 + qa;
           uint2 wv[2 * NCI];
 #pragma unroll
