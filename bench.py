@@ -17,8 +17,9 @@ and bracketed by a barrier and a device synchronisation on both sides, CUDA
 events on the launching stream, max over ranks.  The dominant kernel of the
 path is bracketed by its own CUDA events inside the replayed graph (through the
 library's profiling hook), which gives its average launch duration for the
-roofline.  ``e2e`` repeats the measurement with each step's x copied in from
-pinned host memory and y copied back out, inside the timed region.
+roofline.  ``e2e`` repeats the measurement with each step's x (every layer's
+tokens, one pinned block) copied in from host memory and y copied back out, one
+copy each way per step, inside the timed region.
 
 Multi-GPU (torchrun): every rank runs the same workload on its own GPU (data
 parallel replicas, no collective on the data path); ``value`` counts the
@@ -289,10 +290,13 @@ def run_ours(args, rank, world, dev):
     stream = torch.cuda.Stream(device=dev)
 
     weights = [device_weights(w, L, dev) for L in range(layers)]
-    xh = [host_x(w, replica_layer(L, rank)).pin_memory() for L in range(layers)]
-    xd = [t.to(dev) for t in xh]
-    yd = [torch.empty_like(t) for t in xd]
-    yh = [torch.empty_like(t).pin_memory() for t in xh]
+    # one pinned host block and one device block for all layers' tokens, so an
+    # end-to-end step moves its inputs and results in one copy each way
+    xh_all = torch.stack([host_x(w, replica_layer(L, rank)) for L in range(layers)]).pin_memory()
+    xd_all = xh_all.to(dev)
+    yd_all = torch.empty_like(xd_all)
+    yh_all = torch.empty_like(xh_all).pin_memory()
+    xh, xd, yd, yh = list(xh_all), list(xd_all), list(yd_all), list(yh_all)
     ctx = moe.MoeLayer(w.d, w.E, w.I, w.k, w.T, x_dtype=moe.MOE_F32 if w.x_dtype == "f32" else moe.MOE_BF16,
                        has_router_bias=w.skewed, has_shared=w.I_s > 0)
     path = moe.MOE_PATH_AUTO if args.path == "auto" else (moe.MOE_PATH_GEMV if args.path == "gemv"
@@ -312,9 +316,9 @@ def run_ours(args, rank, world, dev):
             # every launch of the step is the dominant kernel: bracket the
             # step's back-to-back launches with one event pair
             moe.moe_record_event(ev_pair[0], stream)
+        if e2e:
+            xd_all.copy_(xh_all, non_blocking=True)
         for L in range(layers):
-            if e2e:
-                xd[L].copy_(xh[L], non_blocking=True)
             if ev_pair is not None and L == 0 and not whole_layer:
                 moe.moe_time_kernel(ctx.ctx, dom, *ev_pair)
             p = weights[L]
@@ -323,8 +327,8 @@ def run_ours(args, rank, world, dev):
                 moe.moe_set_prefetch(ctx.ctx, q["router_w"], q["shared"])
             moe.moe_forward(ctx.ctx, xd[L], p["router_w"], p["router_b"], p["gate_up"], p["down"], p["shared"], w.k,
                             yd[L], stream)
-            if e2e:
-                yh[L].copy_(yd[L], non_blocking=True)
+        if e2e:
+            yh_all.copy_(yd_all, non_blocking=True)
         if ev_pair is not None and whole_layer:
             moe.moe_record_event(ev_pair[1], stream)
 
