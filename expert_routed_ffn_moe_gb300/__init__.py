@@ -20,7 +20,7 @@ MOE_F32, MOE_BF16 = 0, 1
 MOE_PATH_AUTO, MOE_PATH_GEMV, MOE_PATH_GEMM = 0, 1, 2
 MOE_ROUTER_AUTO, MOE_ROUTER_SIMT, MOE_ROUTER_TENSOR = 0, 1, 2
 (MOE_K_ROUTER, MOE_K_SELECT, MOE_K_GROUP, MOE_K_GEMV_GATE_UP, MOE_K_GEMV_DOWN, MOE_K_GEMM_GATE_UP, MOE_K_GEMM_DOWN,
- MOE_K_COMBINE, MOE_K_DECODE_FUSED, MOE_K_PERMUTE) = range(10)
+ MOE_K_COMBINE, MOE_K_DECODE_FUSED) = range(9)
 
 HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "moe.h")
 

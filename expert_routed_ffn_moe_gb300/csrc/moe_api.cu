@@ -144,7 +144,7 @@ cudaError_t launch(moe_ctx* ctx, int id, cudaStream_t st, F&& f) {
 
 // Steps 1-4 on the device: logits, selection, grouping.
 int run_route(moe_ctx* ctx, const Shapes& s, const void* x, const float* wr, const float* rb, bool tensor,
-              const GemmMaps* maps, cudaStream_t st) {
+              const GemmMaps* maps, cudaStream_t st, bool permute_rows = false) {
   const DevCtl ctl = devctl(ctx);
   cudaError_t err;
   int parts = 1;
@@ -162,7 +162,7 @@ int run_route(moe_ctx* ctx, const Shapes& s, const void* x, const float* wr, con
   }
   err = launch(ctx, MOE_K_SELECT, st, [&] { return launch_select(s, rb, parts, sc, ctl, st); });
   if (err != cudaSuccess) return cuda_fail(err);
-  err = launch(ctx, MOE_K_GROUP, st, [&] { return launch_group(s, sc, ctl, st); });
+  err = launch(ctx, MOE_K_GROUP, st, [&] { return launch_group(s, sc, ctl, st, permute_rows ? x : nullptr); });
   ctx->launches += 1;  // the group step is two kernels
   return cuda_fail(err);
 }
@@ -358,7 +358,7 @@ int moe_inject_stall(moe_ctx* ctx, int on) {
 }
 
 int moe_time_kernel(moe_ctx* ctx, int kernel_id, void* ev_start, void* ev_stop) {
-  if (!ctx || kernel_id < MOE_K_ROUTER || kernel_id > MOE_K_PERMUTE || !ev_start || !ev_stop) return MOE_ERR_ARG;
+  if (!ctx || kernel_id < MOE_K_ROUTER || kernel_id > MOE_K_DECODE_FUSED || !ev_start || !ev_stop) return MOE_ERR_ARG;
   ctx->timed_kernel = kernel_id;
   ctx->ev_start = static_cast<cudaEvent_t>(ev_start);
   ctx->ev_stop = static_cast<cudaEvent_t>(ev_stop);
@@ -449,12 +449,11 @@ int moe_forward(moe_ctx* ctx, const void* x, int T, const float* router_w, const
   if ((rc = make_map(ctx, &maps.shared_gu, sgu, s.d, 2 * s.I, 64, 128)) != MOE_OK) return rc;
   if ((rc = make_map(ctx, &maps.shared_down, sdn, s.I, s.d, 64, 256)) != MOE_OK) return rc;
 
-  if ((rc = run_route(ctx, s, x, router_w, router_b, tensor, &maps, st)) != MOE_OK) return rc;
+  // routing, grouping, and the token rows written in grouped order (x_perm)
+  if ((rc = run_route(ctx, s, x, router_w, router_b, tensor, &maps, st, true)) != MOE_OK) return rc;
   const Scratch& sc = ctx->sc;
   const int sms = ctx->num_sms;
-  cudaError_t err = launch(ctx, MOE_K_PERMUTE, st, [&] { return launch_permute_rows(s, x, sc, ctl, st); });
-  if (err == cudaSuccess)
-    err = launch(ctx, MOE_K_GEMM_GATE_UP, st, [&] { return launch_gemm_gate_up(s, maps, sc, ctl, sms, st); });
+  cudaError_t err = launch(ctx, MOE_K_GEMM_GATE_UP, st, [&] { return launch_gemm_gate_up(s, maps, sc, ctl, sms, st); });
   if (err == cudaSuccess)
     err = launch(ctx, MOE_K_GEMM_DOWN, st, [&] { return launch_gemm_down(s, maps, sc, ctl, sms, st); });
   if (err == cudaSuccess) err = launch(ctx, MOE_K_COMBINE, st, [&] { return launch_combine(s, y, sc, st); });

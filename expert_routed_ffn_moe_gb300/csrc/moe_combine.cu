@@ -1,5 +1,4 @@
-// Expert-grouped copy of the token rows that feeds the gate/up GEMM, and the
-// weighted combine of the grouped-GEMM path.
+// The weighted combine of the grouped-GEMM path.
 //
 // "Optimizing on-device inference for Apple Silicon", section "Reducing
 // intermediate and state traffic": the experts' output projections are
@@ -9,45 +8,6 @@
 #include "moe_internal.h"
 
 namespace moe {
-
-// Token rows in expert-grouped order for the gate/up GEMM: x_perm[p] = x[perm[p]]
-// (rounded to bf16 when x is fp32).  One warp per grouped row, 16-byte stores.
-template <bool XBF16>
-__global__ void __launch_bounds__(256) permute_rows_kernel(Shapes s, const void* __restrict__ x, Scratch sc,
-                                                           DevCtl ctl) {
-  const int lane = threadIdx.x & 31;
-  const long long p = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
-  const long long rows = (long long)s.T * s.k + (s.has_shared ? s.T : 0);
-  if (p >= rows) return;
-  int t = sc.perm[p];
-  if (t < 0 || t >= s.T) {
-    if (lane == 0) raise_status(ctl, kStatusBounds);
-    t = 0;
-  }
-  uint4* dst = reinterpret_cast<uint4*>(sc.x_perm + (size_t)p * s.d);
-  if (XBF16) {
-    const uint4* src = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(x) + (size_t)t * s.d);
-    for (int c = lane; c < s.d / 8; c += 32) __stcs(dst + c, __ldg(src + c));
-  } else {
-    const float4* src = reinterpret_cast<const float4*>(static_cast<const float*>(x) + (size_t)t * s.d);
-    for (int c = lane; c < s.d / 8; c += 32) {
-      const float4 a = __ldg(src + 2 * c), b = __ldg(src + 2 * c + 1);
-      __stcs(dst + c, make_uint4(pack_bf16x2(a.x, a.y), pack_bf16x2(a.z, a.w), pack_bf16x2(b.x, b.y),
-                                 pack_bf16x2(b.z, b.w)));
-    }
-  }
-}
-
-cudaError_t launch_permute_rows(const Shapes& s, const void* x, const Scratch& sc, const DevCtl& ctl,
-                                cudaStream_t st) {
-  const long long rows = (long long)s.T * s.k + (s.has_shared ? s.T : 0);
-  const int blocks = (int)((rows + 7) / 8);
-  if (s.x_bf16)
-    permute_rows_kernel<true><<<blocks, 256, 0, st>>>(s, x, sc, ctl);
-  else
-    permute_rows_kernel<false><<<blocks, 256, 0, st>>>(s, x, sc, ctl);
-  return cudaGetLastError();
-}
 
 // One warp per (token, 256-column slice); each lane owns 8 consecutive columns
 // and reads them with one 16-byte load per contributing row.

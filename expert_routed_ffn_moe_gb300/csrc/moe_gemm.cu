@@ -22,7 +22,7 @@
 //              output row per thread), then SwiGLU -> bf16 h, bf16 expert
 //              outputs, or fp32 router logits;
 // The gate/up GEMM reads its token rows from a copy of x already permuted
-// into expert groups (moe_combine.cu, permute_rows_kernel): gathering 128-byte
+// into expert groups (moe_route.cu, group_scatter_rows_kernel): gathering 128-byte
 // row pieces inside the main loop, by TMA tile::gather4 or by cp.async from
 // helper warps, measured several times slower than streaming contiguous tiles.
 // Two accumulators let the epilogue of tile i overlap the main loop of tile

@@ -64,7 +64,9 @@ cudaError_t launch_router_logits_simt(const Shapes& s, const void* x, const floa
 cudaError_t launch_router_split_weights(const Shapes& s, const float* wr, const Scratch& sc, cudaStream_t st);
 cudaError_t launch_select(const Shapes& s, const float* rb, int logit_parts, const Scratch& sc,
                           const DevCtl& ctl, cudaStream_t st);
-cudaError_t launch_group(const Shapes& s, const Scratch& sc, const DevCtl& ctl, cudaStream_t st);
+// x_rows non-null: also write every token's row, in bf16, to its grouped rows of sc.x_perm
+cudaError_t launch_group(const Shapes& s, const Scratch& sc, const DevCtl& ctl, cudaStream_t st,
+                         const void* x_rows = nullptr);
 cudaError_t launch_export_route(const Shapes& s, const Scratch& sc, int32_t* idx, float* w, int32_t* counts,
                                 int32_t* offsets, int32_t* perm, cudaStream_t st);
 
@@ -111,8 +113,6 @@ cudaError_t launch_decode_fused(const Shapes& s, const void* x, const float* wr,
                                 bool overlap = false);
 
 // moe_combine.cu
-cudaError_t launch_permute_rows(const Shapes& s, const void* x, const Scratch& sc, const DevCtl& ctl,
-                                cudaStream_t st);
 cudaError_t launch_combine(const Shapes& s, void* y, const Scratch& sc, cudaStream_t st);
 
 }  // namespace moe

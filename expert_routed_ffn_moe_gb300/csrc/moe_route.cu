@@ -357,12 +357,75 @@ __global__ void __launch_bounds__(256) group_scatter_kernel(Shapes s, Scratch sc
   }
 }
 
-cudaError_t launch_group(const Shapes& s, const Scratch& sc, const DevCtl& ctl, cudaStream_t st) {
+// The scatter fused with the row permutation of the grouped GEMM path: one
+// warp per token computes the grouped positions of its k picks (as above),
+// reads the token's x row once, and writes it, in bf16, to each of those rows
+// of x_perm and to its shared-expert row -- instead of a scatter kernel that
+// writes perm and a second pass that gathers x by perm.
+template <bool XBF16>
+__global__ void __launch_bounds__(256) group_scatter_rows_kernel(Shapes s, const void* __restrict__ x, Scratch sc,
+                                                                 DevCtl ctl) {
+  const int lane = threadIdx.x & 31;
+  const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
+  if (t >= s.T) return;
+  const int c = t / kChunk, tl = t - c * kChunk;
+  const int nchunk = (s.T + kChunk - 1) / kChunk;
+  int pos = -1;
+  if (lane < s.k) {
+    const int e = sc.idx[(size_t)t * s.k + lane];
+    if (e < 0 || e >= s.E) {
+      raise_status(ctl, kStatusBounds);
+    } else {
+      const unsigned m = sc.chunk_mask[(size_t)c * s.E + e];
+      pos = sc.offsets[e] + sc.chunk_base[(size_t)e * nchunk + c] + __popc(m & ((1u << tl) - 1u));
+      sc.perm[pos] = t;
+      sc.slot[(size_t)t * s.k + lane] = pos;
+    }
+  }
+  const long long shared_row = s.has_shared ? (long long)s.T * s.k + t : -1;
+  if (lane == 0 && shared_row >= 0) sc.perm[shared_row] = t;
+  // the row in 16-byte pieces of 8 bf16: lane takes pieces lane + 32 i
+  const int pieces = s.d / 8;
+  for (int p0 = 0; p0 < pieces; p0 += 32 * 8) {
+    uint4 v[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int pc = p0 + lane + 32 * i;
+      if (pc < pieces) {
+        if (XBF16) {
+          v[i] = __ldg(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(x) + (size_t)t * s.d) + pc);
+        } else {
+          const float4* src = reinterpret_cast<const float4*>(static_cast<const float*>(x) + (size_t)t * s.d);
+          const float4 a = __ldg(src + 2 * pc), b = __ldg(src + 2 * pc + 1);
+          v[i] = make_uint4(pack_bf16x2(a.x, a.y), pack_bf16x2(a.z, a.w), pack_bf16x2(b.x, b.y), pack_bf16x2(b.z, b.w));
+        }
+      }
+    }
+    for (int j = -1; j < s.k; ++j) {
+      const long long row = (j < 0) ? shared_row : (long long)__shfl_sync(0xffffffffu, pos, j);
+      if (row < 0) continue;
+      uint4* dst = reinterpret_cast<uint4*>(sc.x_perm + (size_t)row * s.d);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int pc = p0 + lane + 32 * i;
+        if (pc < pieces) __stcs(dst + pc, v[i]);
+      }
+    }
+  }
+}
+
+cudaError_t launch_group(const Shapes& s, const Scratch& sc, const DevCtl& ctl, cudaStream_t st,
+                         const void* x_rows) {
   const int nchunk = (s.T + kChunk - 1) / kChunk;
   group_scan_kernel<<<(s.E + 7) / 8, 256, 0, st>>>(s, sc);
   cudaError_t err = cudaGetLastError();
   if (err != cudaSuccess) return err;
-  group_scatter_kernel<<<nchunk, 256, 0, st>>>(s, sc, ctl);
+  if (!x_rows)
+    group_scatter_kernel<<<nchunk, 256, 0, st>>>(s, sc, ctl);
+  else if (s.x_bf16)
+    group_scatter_rows_kernel<true><<<(s.T + 7) / 8, 256, 0, st>>>(s, x_rows, sc, ctl);
+  else
+    group_scatter_rows_kernel<false><<<(s.T + 7) / 8, 256, 0, st>>>(s, x_rows, sc, ctl);
   return cudaGetLastError();
 }
 

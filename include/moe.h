@@ -164,14 +164,14 @@ int moe_set_spin_limit(moe_ctx* ctx, long long limit);
 /* Kernel ids for moe_time_kernel. */
 #define MOE_K_ROUTER 0         /* router logits (fp32 FMA or tensor-core) */
 #define MOE_K_SELECT 1         /* top-k selection and weights */
-#define MOE_K_GROUP 2          /* prefix over chunks/experts and the stable scatter */
+#define MOE_K_GROUP 2          /* prefix over chunks/experts and the stable scatter (on the grouped-GEMM
+                                  path the scatter also writes the token rows in grouped order) */
 #define MOE_K_GEMV_GATE_UP 3   /* GEMV path: gate/up projections + SwiGLU */
 #define MOE_K_GEMV_DOWN 4      /* GEMV path: down projection + weighted combine + shared */
 #define MOE_K_GEMM_GATE_UP 5   /* grouped GEMM: gate/up projections + SwiGLU */
 #define MOE_K_GEMM_DOWN 6      /* grouped GEMM: down projection */
 #define MOE_K_COMBINE 7        /* grouped-GEMM path: weighted combine + shared */
 #define MOE_K_DECODE_FUSED 8   /* small-T path: the whole layer in one cooperative kernel */
-#define MOE_K_PERMUTE 9        /* grouped-GEMM path: token rows copied into expert-grouped order */
 
 /* Profiling hook: the next moe_forward/moe_route call on `ctx` records the
  * CUDA events `ev_start` / `ev_stop` (cudaEvent_t, created by the caller with

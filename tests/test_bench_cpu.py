@@ -1,0 +1,34 @@
+"""Host-side logic of bench.py that needs no GPU: the traffic record lookup
+(an ncu figure is reported only for the kernel source it was taken of) and
+the multi-rank aggregation."""
+import os
+import shutil
+
+import pytest
+
+import bench
+
+
+def test_traffic_record_matches_only_current_source(tmp_path, monkeypatch):
+    # a private copy of the sources and profiles: changing a byte of the
+    # kernel source must void the recorded traffic
+    root = tmp_path / "repo"
+    shutil.copytree(bench.CSRC, root / "expert_routed_ffn_moe_gb300" / "csrc")
+    (root / "profiles").mkdir()
+    monkeypatch.setattr(bench, "HERE", str(root))
+    monkeypatch.setattr(bench, "CSRC", str(root / "expert_routed_ffn_moe_gb300" / "csrc"))
+    h = bench.kernel_source_hash("decode_fused_kernel")
+    (root / "profiles" / "k.md").write_text(
+        f"text\ntraffic-record: kernel=decode_fused_kernel source_sha256={h} bytes_per_launch=12345\n")
+    assert bench.profiled_traffic("decode_fused_kernel") == 12345
+    assert bench.profiled_traffic("grouped_gemm_kernel<gate_up>") is None
+    src = root / "expert_routed_ffn_moe_gb300" / "csrc" / "moe_decode.cu"
+    src.write_text(src.read_text() + "\n// changed\n")
+    assert bench.profiled_traffic("decode_fused_kernel") is None
+
+
+def test_aggregate_single_rank():
+    value, ms_step, e2e = bench.aggregate(ms=100.0, ms_e2e=200.0, steps=10, tokens_per_step=5, world=1, dev=None)
+    assert ms_step == pytest.approx(10.0)
+    assert value == pytest.approx(5 / 0.010)
+    assert e2e == pytest.approx(5 / 0.020)

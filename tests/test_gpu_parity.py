@@ -267,3 +267,19 @@ def test_overlapped_decode_launches_match_plain():
     layer.close()
     for o in outs[1:]:
         assert torch.equal(o, outs[0])
+
+
+def test_prefetch_hint_does_not_change_results():
+    # moe_set_prefetch only moves the next layer's weights into L2: the layer
+    # computed with the hint must equal the one computed without it, bitwise.
+    w = W["decode"]
+    d0, d1 = device_inputs(w, layer_inputs(w, 0)), device_inputs(w, layer_inputs(w, 1))
+    layer = make_layer(w)
+    args = (d0["router_w"], d0["router_b"], d0["gate_up"], d0["down"], d0["shared"])
+    y_plain = layer.forward(d0["x"], *args).clone()
+    moe.moe_set_prefetch(layer.ctx, d1["router_w"], d1["shared"])
+    y_hint = layer.forward(d0["x"], *args).clone()
+    torch.cuda.synchronize()
+    assert layer.status() == moe.MOE_OK
+    layer.close()
+    assert torch.equal(y_plain, y_hint)
