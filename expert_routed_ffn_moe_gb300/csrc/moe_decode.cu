@@ -355,8 +355,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const DecodeA
       }
       __syncthreads();
     }
-    // shared-expert gate/up + SwiGLU: item q < n_sh goes to warp q mod kWarps
-    for (int q = warp; q < n_sh; q += kWarps) {
+    // shared-expert gate/up + SwiGLU: item q < n_sh goes to warp kWarps - 1 - (q
+    // mod kWarps), the last warps, so that the selection warps of phase B (warp
+    // t for token t) start polling the logits while these units are computed
+    for (int q = kWarps - 1 - warp; q < n_sh; q += kWarps) {
       const int slot = q % A.ring_slots;
       if (!wait_item(full, slot_issued, q, A.ring_slots, A.ctl)) {
         flag_s = 0;
@@ -432,12 +434,30 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const DecodeA
           sc.idx[(size_t)t * s.k + rank] = pe;
           sc.w[(size_t)t * s.k + rank] = pw;
         }
+        if (MAXT == 1) {
+          // batch 1: the active experts are the picks in ascending id (rank
+          // order), grouped h row = rank, then the shared expert (row k)
+          act_e[rank] = pe;
+          act_m[rank] = 1u;
+          act_row[rank] = rank;
+          act_w[rank][0] = pw;
+        }
+      }
+      if (MAXT == 1 && lane == 0) {
+        if (s.has_shared) {
+          act_e[s.k] = s.E;
+          act_m[s.k] = 1u;
+          act_row[s.k] = s.k;
+          act_w[s.k][0] = 1.f;
+        }
+        n_act_s = s.k + (s.has_shared ? 1 : 0);
       }
     }
   }
   __syncthreads();
   ok = flag_s != 0;
   if (ok) {
+    if (MAXT > 1) {
     // group tokens by expert: masks, active list (ascending), grouped h rows
     unsigned m = 0u;
     if (tid < s.E) {
@@ -485,6 +505,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const DecodeA
       }
     }
     __syncthreads();
+    }
     const int n_act = n_act_s;
     const int n_routed = n_act - (s.has_shared ? 1 : 0);
     const int units = n_routed * s.I;
