@@ -467,8 +467,8 @@ int moe_status(moe_ctx* ctx) {
   if (cudaMemcpy(&v, ctx->sc.status, 4, cudaMemcpyDeviceToHost) != cudaSuccess) return MOE_ERR_CUDA;
   if (v && cudaMemset(ctx->sc.status, 0, 4) != cudaSuccess) return MOE_ERR_CUDA;
   // nothing to repair after a timeout: every block of a decode launch that gave
-  // up still leaves through the exit counter, and the next launch tags its
-  // values with a new epoch, so nothing the failed launch wrote is taken as ready
+  // up still publishes the launch's epoch, and the next launch tags its values
+  // with a new one, so nothing the failed launch wrote is taken as ready
   if (v & kStatusTimeout) return MOE_ERR_TIMEOUT;
   if (v & kStatusBounds) return MOE_ERR_BOUNDS;
   return MOE_OK;

@@ -125,7 +125,7 @@ struct DecodeArgs {
   void* y;
   Scratch sc;
   DevCtl ctl;
-  unsigned* bar;   // [0] exit counter, [1] epoch of the last launch
+  unsigned* bar;   // [1]: epoch of the last launch ([0] unused)
   // optional prefetch hint: weights the next layer reads first (may be null)
   const float* next_wr;
   const uint16_t* next_shared;
@@ -721,17 +721,13 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const DecodeA
   // wait (bounded) for every issued item before the shared memory is released
   __syncthreads();
   if (flag_s == 0 && tid < A.ring_slots) drain_slot(full, slot_issued, tid, A.ctl);
-  // leave: the last block out publishes this launch's epoch (the next launch
-  // tags with epoch + 1) and clears the exit counter
-  __syncthreads();
-  if (tid == 0) {
-    __threadfence();
-    if (atomicAdd(A.bar, 1u) == (unsigned)G - 1) {
-      A.bar[0] = 0u;
-      A.bar[1] = ep_s;
-      __threadfence();
-    }
-  }
+  // leave: publish this launch's epoch (the next launch, which starts after
+  // this grid completes, tags with epoch + 1).  Every block stores the same
+  // value, with no exit counter: no block can leave before every block has
+  // read the old epoch, since each first waits for every block's logits,
+  // which carry it (a block that gives up does so only after the spin limit,
+  // long after all blocks of the cooperative launch have started).
+  if (tid == 0) A.bar[1] = ep_s;
 }
 
 
@@ -928,7 +924,7 @@ constexpr size_t kNoAllocOffLogits = kNoAllocH;
 constexpr size_t kNoAllocOffIdx = kNoAllocOffLogits + kNoAllocLogits;
 constexpr size_t kNoAllocOffW = kNoAllocOffIdx + kNoAllocPicks;
 constexpr size_t kNoAllocOffStatus = kNoAllocOffW + kNoAllocPicks;
-constexpr size_t kNoAllocOffBar = kNoAllocOffStatus + 256;  // exit counter and epoch
+constexpr size_t kNoAllocOffBar = kNoAllocOffStatus + 256;  // epoch of the last launch
 constexpr size_t kNoAllocBarBytes = 256;
 constexpr size_t kNoAllocBytes = kNoAllocOffBar + kNoAllocBarBytes;
 
@@ -945,9 +941,9 @@ std::mutex g_noalloc_mu;
 
 // The scratch array (about 1.3 MB).  Every call shares it and it keeps the
 // last call's contents.  Its zero initial contents are a valid start: tag 0
-// is never a launch's epoch.  The exit counter, which must be zero when a
-// launch starts, is cleared at the start of every call; the epoch word is
-// kept, since a tag left by an earlier call must never match a later one.
+// is never a launch's epoch, and nothing must be cleared between calls (the
+// epoch word is kept, since a tag left by an earlier call must never match a
+// later one).
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocBytes];
 
 extern "C" int moe_decode_noalloc(const void* x, int T, int x_dtype, int d, int n_experts, int inter, int top_k,
@@ -1007,7 +1003,6 @@ extern "C" int moe_decode_noalloc(const void* x, int T, int x_dtype, int d, int 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   unsigned* words = reinterpret_cast<unsigned*>(nd.base + kNoAllocOffStatus);
   unsigned* bar = reinterpret_cast<unsigned*>(nd.base + kNoAllocOffBar);
-  if (cudaMemsetAsync(bar, 0, sizeof(unsigned), st) != cudaSuccess) return MOE_ERR_CUDA;
   Scratch sc{};
   sc.dec_h = reinterpret_cast<float*>(nd.base);
   sc.dec_hreps = 1;

@@ -44,7 +44,7 @@ struct Scratch {
   float* h_gemv;          // [Tg*k + Tg, I] fp32 SwiGLU activations (GEMV path)
   uint16_t* out;          // [T*k + T, d] bf16 expert outputs, grouped rows (GEMM path)
   unsigned* status;       // device status word
-  unsigned* gridbar;      // fused decode kernel: [0] exit counter, [1] epoch of the last launch
+  unsigned* gridbar;      // fused decode kernel: [1] epoch of the last launch
   float* dec_logits;      // fused decode kernel: [dec_reps][T][E] router logits as (fp32, epoch) 64-bit words
   float* dec_h;           // fused decode kernel: [dec_hreps][T*k + T][I] SwiGLU activations as (fp32, epoch) words
   int dec_reps;           // copies of the logits (blocks read copy b % reps)

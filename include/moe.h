@@ -223,10 +223,10 @@ int moe_inject_stall(moe_ctx* ctx, int on);
  * anything is launched.  The first call on each device looks up the array's
  * device address (cudaGetSymbolAddress) and sets kernel attributes, with that
  * device current: make that first call before any stream capture.  Every call
- * shares the one array, which keeps the previous call's contents (the exit
- * counter that must start at zero is cleared by each call on `stream`), so
- * calls that overlap on the GPU -- on different streams, or from different
- * threads -- race and must not be issued.  Asynchronous on `stream`. */
+ * shares the one array, which keeps the previous call's contents (its zero
+ * start and every later state are valid starts), so calls that overlap on the
+ * GPU -- on different streams, or from different threads -- race and must not
+ * be issued.  Asynchronous on `stream`; one kernel launch per call. */
 int moe_decode_noalloc(const void* x, int T, int x_dtype, int d, int n_experts, int inter, int top_k,
                        const float* router_w, const float* router_b, const void* experts_gate_up,
                        const void* experts_down, const void* shared_w, void* y, unsigned* status, void* stream);
