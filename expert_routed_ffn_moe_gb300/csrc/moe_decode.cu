@@ -14,13 +14,17 @@
 //
 //   phase A  router logits l[t, e] (fp32 FMA, four experts per pass, each row
 //            split over 4 warps and summed in a fixed order), and the shared
-//            expert's gate/up GEMV + SwiGLU, which needs no routing.
+//            expert's gate/up GEMV + SwiGLU, which needs no routing (on the
+//            last warps, so the selection warps go on to phase B).
 //   -- every block waits for all logits --
 //   phase B  every block selects the top-k of every token from the logits
 //            (one warp per token; same result in every block); groups tokens
-//            by expert in shared memory; runs the routed gate/up GEMV +
-//            SwiGLU for its (expert, neuron) units; then loads its phase-C
-//            down rows.
+//            by expert in shared memory (at batch 1 the selection warp writes
+//            the active list itself); streams and runs the routed gate/up
+//            GEMV + SwiGLU for its (expert, neuron) units.  Weight rows of
+//            phases A-C move through a ring of shared-memory slots filled by
+//            TMA bulk copies; the down rows of phase C enter it behind the
+//            last gate/up units.
 //   -- every block waits for all of h --
 //   phase C  one warp per output feature: for the active experts in ascending
 //            id (shared expert last) the down-projection row, dotted with each
@@ -36,8 +40,8 @@
 // starts on the logits one L2 round trip after the last of them lands, instead
 // of after a barrier's arrive, poll and release and then a separate load.
 // (Per-block "h written" flags behind a fence measured slower: the fence waits
-// out the block's in-flight traffic.)  The last block to leave publishes the
-// launch's epoch; the next launch, a graph replay included, tags with the one
+// out the block's in-flight traffic.)  Every block stores the launch's epoch
+// as it leaves; the next launch, a graph replay included, tags with the one
 // after it.
 #include <math.h>
 
