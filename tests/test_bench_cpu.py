@@ -23,7 +23,9 @@ def test_traffic_record_matches_only_current_source(tmp_path, monkeypatch):
     assert bench.profiled_traffic("decode_fused_kernel") == 12345
     assert bench.profiled_traffic("grouped_gemm_kernel<gate_up>") is None
     src = root / "expert_routed_ffn_moe_gb300" / "csrc" / "moe_decode.cu"
-    src.write_text(src.read_text() + "\n// changed\n")
+    src.write_text(src.read_text() + "\n// a comment changes no kernel\n")
+    assert bench.profiled_traffic("decode_fused_kernel") == 12345
+    src.write_text(src.read_text() + "\nstatic int changed_code = 1;\n")
     assert bench.profiled_traffic("decode_fused_kernel") is None
 
 
