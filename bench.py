@@ -305,8 +305,11 @@ def run_ours(args, rank, world, dev):
     yd_all = torch.empty_like(xd_all)
     yh_all = torch.empty_like(xh_all).pin_memory()
     xh, xd, yd, yh = list(xh_all), list(xd_all), list(yd_all), list(yh_all)
-    ctx = moe.MoeLayer(w.d, w.E, w.I, w.k, w.T, x_dtype=moe.MOE_F32 if w.x_dtype == "f32" else moe.MOE_BF16,
+    max_tokens = args.chunk if args.chunk else w.T
+    ctx = moe.MoeLayer(w.d, w.E, w.I, w.k, max_tokens, x_dtype=moe.MOE_F32 if w.x_dtype == "f32" else moe.MOE_BF16,
                        has_router_bias=w.skewed, has_shared=w.I_s > 0)
+    if args.chunk:  # chunked prefill: workspace for `chunk` tokens, the layer over all T in slices
+        moe.moe_set_chunk_tokens(ctx.ctx, args.chunk)
     path = moe.MOE_PATH_AUTO if args.path == "auto" else (moe.MOE_PATH_GEMV if args.path == "gemv"
                                                           else moe.MOE_PATH_GEMM)
     moe.moe_set_path(ctx.ctx, path)
@@ -345,8 +348,10 @@ def run_ours(args, rank, world, dev):
     with torch.cuda.stream(stream):
         for L in range(layers):
             p = weights[L]
-            r = ctx.route(xd[L], p["router_w"], p["router_b"], stream=stream)
-            costs.append(layer_costs(w, r["idx"].cpu().numpy()))
+            step_t = args.chunk or w.T  # moe_route keeps the T <= max_tokens limit: route slice by slice
+            idx = [ctx.route(xd[L][t0:t0 + step_t], p["router_w"], p["router_b"], stream=stream)["idx"].cpu().numpy()
+                   for t0 in range(0, w.T, step_t)]
+            costs.append(layer_costs(w, np.concatenate(idx)))
         for _ in range(max(args.warmup, 0)):
             step()
     stream.synchronize()
@@ -449,6 +454,14 @@ def run_ours(args, rank, world, dev):
     layer_bytes = statistics.mean(c["layer_bytes"] for c in costs)
     layer_flops = statistics.mean(c["layer_flops"] for c in costs)
     ms_layer = ms_step / layers
+    if args.chunk and args.chunk < w.T:
+        # chunked: the event hook times one slice's launch, not the layer's; report the
+        # whole layer against the layer's minimum bytes (weights read once), which the
+        # chunked run exceeds by design (the selected experts are read once per slice)
+        gbs = layer_bytes / (ms_layer / 1e3) / 1e9
+        roof = dict(bound="hbm", achieved=round(gbs, 1), peak=peaks["hbm_gbs"], unit="GB/s",
+                    frac=round(gbs / peaks["hbm_gbs"], 4), traffic=None, kernel="whole layer, chunked",
+                    algorithmic_bytes_per_launch=int(layer_bytes), peak_source=peaks["source"])
     whole = dict(ms_per_layer=round(ms_layer, 5),
                  hbm_frac_of_layer=round(layer_bytes / (ms_layer / 1e3) / 1e9 / peaks["hbm_gbs"], 4),
                  tensor_frac_of_layer=round(layer_flops / (ms_layer / 1e3) / 1e12 / peaks["bf16_tflops"], 4),
@@ -475,7 +488,7 @@ def run_ours(args, rank, world, dev):
                                    if layer_bytes * layers > L2_BYTES else
                                    f"inputs fit in L2 ({layer_bytes * layers / 1e6:.0f} MB per step): "
                                    f"a profiling run, not a bench number"),
-                               parallelism=f"replicas x{world}"),
+                               parallelism=f"replicas x{world}", **({"chunk_tokens": args.chunk} if args.chunk else {})),
                    e2e=dict(value=round(e2e_value, 1), unit=UNIT,
                             h2d_bytes_per_step=int(sum(t.numel() * t.element_size() for t in xh)),
                             d2h_bytes_per_step=int(sum(t.numel() * t.element_size() for t in yh))),
@@ -529,6 +542,8 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--ref-step-seconds", type=float, default=3.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--chunk", type=int, default=0,
+                    help="chunked prefill: size the workspace for this many tokens and run T in slices")
     ap.add_argument("--layers", type=int, default=0,
                     help="stacked layers per step (default: the workload's own; fewer only for small profiling runs)")
     args = ap.parse_args()

@@ -55,6 +55,8 @@ def lib() -> ctypes.CDLL:
         L.moe_set_spin_limit.argtypes = [P, ctypes.c_longlong]
         L.moe_record_event.argtypes = [P, P]
         L.moe_record_event.restype = I
+        L.moe_set_chunk_tokens.argtypes = [P, I]
+        L.moe_set_chunk_tokens.restype = I
         L.moe_set_overlap.argtypes = [P, I]
         L.moe_set_overlap.restype = I
         L.moe_set_prefetch.argtypes = [P, P, P]
@@ -144,6 +146,12 @@ def moe_set_spin_limit(ctx, limit_ns: int) -> None:
 def moe_record_event(event, stream=None) -> None:
     """Record a torch.cuda.Event on a stream; timeable also under graph capture."""
     _check(lib().moe_record_event(ctypes.c_void_p(event.cuda_event), _stream(stream)), "moe_record_event")
+
+
+def moe_set_chunk_tokens(ctx, chunk: int) -> None:
+    """Chunked prefill (see moe.h): with chunk > 0 moe_forward accepts any T and runs
+    slices of at most `chunk` tokens through the context's bounded workspace."""
+    _check(lib().moe_set_chunk_tokens(ctx, int(chunk)), "moe_set_chunk_tokens")
 
 
 def moe_set_overlap(ctx, on: bool) -> None:

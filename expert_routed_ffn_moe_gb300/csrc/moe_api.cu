@@ -25,6 +25,7 @@ struct moe_ctx {
   int stall = 0;            // test hook (moe_inject_stall)
   const float* next_wr = nullptr;         // prefetch hint for the next call (moe_set_prefetch)
   bool overlap = false;                   // programmatic launch overlap (moe_set_overlap)
+  int chunk = 0;                          // chunked prefill: tokens per slice (moe_set_chunk_tokens), 0 = off
   const uint16_t* next_shared = nullptr;
   int gemv_max_t = 0;       // largest T the GEMV kernels accept for this shape (0: none)
   int decode_max_t = 0;     // largest T the fused decode kernel accepts (0: none)
@@ -388,9 +389,42 @@ int moe_route(moe_ctx* ctx, const void* x, int T, const float* router_w, const f
   return cuda_fail(launch_export_route(s, ctx->sc, idx, w, counts, offsets, perm, st));
 }
 
+static int forward_one(moe_ctx* ctx, const void* x, int T, const float* router_w, const float* router_b,
+                       const void* experts_gate_up, const void* experts_down, const void* shared_w, int top_k,
+                       void* y, void* stream);
+
+int moe_set_chunk_tokens(moe_ctx* ctx, int chunk) {
+  if (!ctx || chunk < 0 || chunk > ctx->cfg.max_tokens) return MOE_ERR_ARG;
+  ctx->chunk = chunk;
+  return MOE_OK;
+}
+
 int moe_forward(moe_ctx* ctx, const void* x, int T, const float* router_w, const float* router_b,
                 const void* experts_gate_up, const void* experts_down, const void* shared_w, int top_k, void* y,
                 void* stream) {
+  if (!ctx || T < 0) return MOE_ERR_ARG;
+  const int chunk = ctx->chunk;
+  if (chunk == 0 || T <= chunk)
+    return forward_one(ctx, x, T, router_w, router_b, experts_gate_up, experts_down, shared_w, top_k, y, stream);
+  // Chunked prefill: tokens are independent, so the layer over T tokens is the
+  // layer over consecutive slices of at most `chunk` tokens, each through the
+  // context's workspace (sized for max_tokens) -- exact, at the price of
+  // reading the selected experts' weights once per slice.
+  if (!x || !y) return MOE_ERR_ARG;
+  const size_t row = (size_t)ctx->cfg.d * (ctx->cfg.x_dtype == MOE_BF16 ? 2 : 4);
+  for (int t0 = 0; t0 < T; t0 += chunk) {
+    const int n = T - t0 < chunk ? T - t0 : chunk;
+    const int rc = forward_one(ctx, static_cast<const char*>(x) + (size_t)t0 * row, n, router_w, router_b,
+                               experts_gate_up, experts_down, shared_w, top_k, static_cast<char*>(y) + (size_t)t0 * row,
+                               stream);
+    if (rc != MOE_OK) return rc;
+  }
+  return MOE_OK;
+}
+
+static int forward_one(moe_ctx* ctx, const void* x, int T, const float* router_w, const float* router_b,
+                       const void* experts_gate_up, const void* experts_down, const void* shared_w, int top_k,
+                       void* y, void* stream) {
   int rc = check_route_args(ctx, x, T, router_w, router_b, top_k);
   if (rc != MOE_OK || T == 0) return rc;
   const moe_config& c = ctx->cfg;

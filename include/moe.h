@@ -149,6 +149,19 @@ int moe_set_prefetch(moe_ctx* ctx, const float* next_router_w, const void* next_
  * MOE_ERR_ARG on other values. */
 int moe_set_overlap(moe_ctx* ctx, int on);
 
+/* Chunked prefill with bounded workspace ("Optimizing on-device inference for
+ * Apple Silicon", section on bounding temporary memory by splitting the prompt
+ * into chunks: a long prompt runs as a sequence of bounded chunks whose
+ * temporary buffers are reused, so working memory does not grow with it).
+ * With chunk > 0, moe_forward accepts any T >= 0 (not only T <= max_tokens)
+ * and runs the layer on consecutive slices of at most `chunk` tokens through
+ * the context's workspace, which stays sized for max_tokens.  The result is
+ * the layer over all T tokens (tokens are independent; each slice may take
+ * its own path by size); the selected experts' weights are read once per
+ * slice.  chunk = 0 (the default) turns it off.  MOE_ERR_ARG if chunk < 0 or
+ * chunk > max_tokens.  moe_route keeps the T <= max_tokens limit. */
+int moe_set_chunk_tokens(moe_ctx* ctx, int chunk);
+
 /* Synchronise the device, then read and clear the context's device status
  * word: MOE_OK, or the first MOE_ERR_TIMEOUT / MOE_ERR_BOUNDS latched by a
  * kernel since the last call; MOE_ERR_CUDA if the synchronisation itself

@@ -283,3 +283,31 @@ def test_prefetch_hint_does_not_change_results():
     assert layer.status() == moe.MOE_OK
     layer.close()
     assert torch.equal(y_plain, y_hint)
+
+
+def test_chunked_prefill_matches_oracle_and_unchunked():
+    # moe_set_chunk_tokens: a context sized for 256 tokens runs T = 700 in
+    # slices of 256, 256 and 188; every token must match the oracle, and the
+    # same tokens through a context sized for all 700 must agree (each slice
+    # takes the grouped-GEMM path, whose per-row arithmetic does not depend on
+    # which other rows share a tile).
+    w = custom("chunked", T=700)
+    inp = layer_inputs(w)
+    d = device_inputs(w, inp)
+    args = (d["router_w"], d["router_b"], d["gate_up"], d["down"], d["shared"])
+    small = make_layer(w, max_tokens=256)
+    moe.moe_set_chunk_tokens(small.ctx, 256)
+    y_chunked = small.forward(d["x"], *args).clone()
+    torch.cuda.synchronize()
+    assert small.status() == moe.MOE_OK
+    with pytest.raises(moe.MoeError):
+        moe.moe_set_chunk_tokens(small.ctx, 257)  # above max_tokens
+    small.close()
+    full = make_layer(w)
+    y_full = full.forward(d["x"], *args).clone()
+    torch.cuda.synchronize()
+    assert full.status() == moe.MOE_OK
+    full.close()
+    assert torch.equal(y_chunked, y_full)
+    toks = sample_tokens(w.T, 48)
+    check_y(y_host(y_chunked)[toks], oracle_y(w, inp, toks), "chunked prefill")
