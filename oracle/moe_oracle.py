@@ -83,10 +83,14 @@ def select_top_k(logits: np.ndarray, k: int):
     return idx, margin
 
 
-def route(logits: np.ndarray, k: int):
-    """Steps 2-4: (idx [T, k] int32 ascending, w [T, k] fp64, margin [T])."""
+def route(logits: np.ndarray, k: int, weight_logits: np.ndarray | None = None):
+    """Steps 2-4: (idx [T, k] int32 ascending, w [T, k] fp64, margin [T]).
+
+    The k experts are picked on ``logits``; their weights come from
+    ``weight_logits`` (default: the same logits).  The variant with a router
+    bias that only balances load picks on l + b and weights on l."""
     idx, margin = select_top_k(logits, k)
-    p = softmax(logits)
+    p = softmax(logits if weight_logits is None else weight_logits)
     p_sel = np.take_along_axis(p, idx.astype(np.int64), axis=1)
     w = p_sel / p_sel.sum(axis=1, keepdims=True)
     return idx, w, margin
@@ -129,7 +133,7 @@ def swiglu_ffn(x_rows: np.ndarray, gate_up: np.ndarray, down: np.ndarray) -> np.
 
 
 def moe_layer(x, router_w, router_b, gate_up, down, shared, k, *, x_bf16: bool,
-              shared_inter: int | None = None, tokens=None, expert_ids=None):
+              shared_inter: int | None = None, tokens=None, expert_ids=None, bias_select_only: bool = False):
     """Steps 1-8 for the token rows ``tokens`` (default: all).
 
     x        [T, d]  fp32 values, or bf16 bits when ``x_bf16``
@@ -138,6 +142,8 @@ def moe_layer(x, router_w, router_b, gate_up, down, shared, k, *, x_bf16: bool,
     shared   flat bf16 bits: gate_up [2I_s, d] then down [d, I_s]; or None
     expert_ids  which expert each of the n stacked matrices is (default
              0..n-1); lets a caller pass only the experts the sampled tokens use.
+    bias_select_only  the router bias picks the experts but their weights are
+             the softmax of the unbiased logits over the picks.
 
     Returns dict(y [n_tok, d] fp64, idx, w, margin, logits) for those tokens."""
     xs = as_f64(x, x_bf16)
@@ -145,7 +151,8 @@ def moe_layer(x, router_w, router_b, gate_up, down, shared, k, *, x_bf16: bool,
     xs = xs[tokens]
     wr = np.asarray(router_w, dtype=np.float64)
     logits = router_logits(xs, wr, router_b)
-    idx, w, margin = route(logits, k)
+    unbiased = router_logits(xs, wr, None) if (bias_select_only and router_b is not None) else None
+    idx, w, margin = route(logits, k, weight_logits=unbiased)
     n_tok, d = xs.shape
     y = np.zeros((n_tok, d), dtype=np.float64)
 

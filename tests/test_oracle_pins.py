@@ -135,6 +135,49 @@ def test_router_bias_only_routing():
     assert np.allclose(w[0], p / p.sum(), atol=1e-15)
 
 
+def test_bias_for_selection_only_hand_worked():
+    # logits ln(1..4), bias +10 on expert 0, k = 2: the bias makes expert 0 a
+    # pick (with expert 3); its weight comes from the unbiased logits:
+    # exp(0) / (exp(0) + 4) = 1/5, expert 3: 4/5.  With the bias in the weights
+    # expert 0 would carry e^10 / (e^10 + 4).
+    l = np.log(np.array([[1.0, 2.0, 3.0, 4.0]]))
+    b = np.array([10.0, 0.0, 0.0, 0.0])
+    idx, w, _ = oracle.route(l + b, 2, weight_logits=l)
+    assert list(idx[0]) == [0, 3]
+    assert abs(w[0, 0] - 0.2) < 1e-15 and abs(w[0, 1] - 0.8) < 1e-15
+    _, w_biased, _ = oracle.route(l + b, 2)
+    assert abs(w_biased[0, 0] - math.exp(10) / (math.exp(10) + 4)) < 1e-15
+
+
+def test_bias_for_selection_only_properties():
+    rng = np.random.default_rng(11)
+    l = rng.normal(size=(40, 16))
+    # no bias: the variant is the plain routing
+    a = oracle.route(l, 4)
+    b = oracle.route(l, 4, weight_logits=l)
+    assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+    # a bias that keeps the picks changes no weight, whatever its size
+    idx0, w0, _ = oracle.route(l, 4)
+    bias = np.zeros(16)
+    for scale in (1e-3, 1e-1):
+        bias_t = scale * rng.normal(size=16)
+        idx1, w1, _ = oracle.route(l + bias_t, 4, weight_logits=l)
+        same = np.all(idx1 == idx0, axis=1)
+        assert np.allclose(w1[same], w0[same], atol=1e-15, rtol=0)
+    # the layer: identical to routing on l + b with weights from the softmax of
+    # the unbiased logits over the picks, written out token by token
+    E, k = 6, 3
+    x, wr, gu, dn, sh = tiny_layer(rng, E=E, k=k)
+    bias = rng.normal(size=E) * 2
+    r = oracle.moe_layer(x, wr, bias, gu, dn, sh, k, x_bf16=False, bias_select_only=True)
+    lu = x.astype(np.float64) @ wr.astype(np.float64).T
+    for t in range(x.shape[0]):
+        chosen = sorted(range(E), key=lambda e: (-(lu[t, e] + bias[e]), e))[:k]
+        z = sum(math.exp(lu[t, e]) for e in chosen)
+        assert list(r["idx"][t]) == sorted(chosen)
+        assert np.allclose(r["w"][t], [math.exp(lu[t, e]) / z for e in sorted(chosen)], atol=1e-14)
+
+
 # ----------------------------------------------------------------- grouping
 
 def brute_group(idx, E):
