@@ -97,6 +97,7 @@ Shapes shapes(const moe_ctx* ctx, int T, int top_k) {
   s.k = top_k;
   s.has_shared = c.has_shared;
   s.x_bf16 = c.x_dtype == MOE_BF16;
+  s.bias_sel = c.has_router_bias && c.bias_select_only;
   return s;
 }
 
@@ -195,6 +196,7 @@ int moe_init(const moe_config* cfg, moe_ctx** out) {
   if (c.top_k > c.n_experts || c.top_k > kMaxTopK) return MOE_ERR_ARG;
   if (c.n_experts > kMaxExperts || c.d % 256 != 0 || c.inter % 128 != 0) return MOE_ERR_UNSUPPORTED;
   if (c.has_shared && c.shared_inter != c.inter) return MOE_ERR_UNSUPPORTED;
+  if (c.bias_select_only != 0 && c.bias_select_only != 1) return MOE_ERR_ARG;
   if ((long long)c.max_tokens * (c.top_k + 1) >= (1LL << 31) / 2) return MOE_ERR_UNSUPPORTED;
 
   int dev = 0;
@@ -217,7 +219,7 @@ int moe_init(const moe_config* cfg, moe_ctx** out) {
   ctx->spin_ns = kDefaultSpinNs;
   ctx->gemv_max_t = gemv_limit(ctx->cfg);
   for (int t = 1; t <= 16 && t <= c.max_tokens; ++t) {
-    Shapes s1;
+    Shapes s1{};
     s1.T = t;
     s1.d = c.d;
     s1.E = c.n_experts;

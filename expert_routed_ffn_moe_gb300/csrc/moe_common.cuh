@@ -135,6 +135,31 @@ MOE_DEV bool warp_top_k(const float (&v)[8], int E, int k, int lane, int& pick_e
   return __all_sync(0xffffffffu, finite);
 }
 
+// The logit of expert e in the warp layout of warp_top_k (lane l holds experts
+// l, l + 32, ..., in u[0..7]); every lane may ask for its own e.
+MOE_DEV float warp_logit_of(const float (&u)[8], int e) {
+  const int src = e & 31, slot = e >> 5;
+  float r = 0.f;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const float x = __shfl_sync(0xffffffffu, u[i], src);
+    if (i == slot) r = x;
+  }
+  return r;
+}
+
+// Weights of the picks from other logits than the ones that chose them (a
+// router bias used only for selection): lane j < k holds pick j's unbiased
+// logit lu; returns exp(lu - max) / sum over the k picks.
+MOE_DEV float warp_pick_weight(float lu, int k, int lane) {
+  float m = lane < k ? lu : -INFINITY;
+  for (int o = k <= 8 ? 4 : 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  const float ex = lane < k ? __expf(lu - m) : 0.f;
+  float den = ex;
+  for (int o = k <= 8 ? 4 : 16; o > 0; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
+  return __fdividef(ex, den);
+}
+
 MOE_DEV uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }

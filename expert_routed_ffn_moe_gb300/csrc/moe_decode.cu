@@ -396,7 +396,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const DecodeA
     // test hook: wait for a tag that no block writes
     const unsigned want = ep_s + (A.ctl.stall ? 1u : 0u);
     for (int t = warp; t < s.T; t += kWarps) {
-      float v[8];
+      float v[8], u[8];  // logits with and without the router bias
 #pragma unroll
       for (int i = 0; i < 8; ++i) v[i] = (A.rb && lane + 32 * i < s.E) ? __ldg(A.rb + lane + 32 * i) : 0.f;
       const long long t0 = clock64(), lim = wait_cycles(A.ctl);
@@ -413,7 +413,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const DecodeA
         for (int i = 0; i < 8; ++i) ready = ready && (lane + 32 * i >= s.E || tag_of(w[i]) == want);
         if (__all_sync(0xffffffffu, ready)) {
 #pragma unroll
-          for (int i = 0; i < 8; ++i) v[i] = (lane + 32 * i < s.E) ? value_of(w[i]) + v[i] : -INFINITY;
+          for (int i = 0; i < 8; ++i) {
+            u[i] = (lane + 32 * i < s.E) ? value_of(w[i]) : -INFINITY;
+            v[i] = (lane + 32 * i < s.E) ? u[i] + v[i] : -INFINITY;
+          }
           break;
         }
         if (polls >= 256 && __any_sync(0xffffffffu, clock64() - t0 > lim)) {
@@ -431,6 +434,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const DecodeA
       int pe, rank;
       float pw;
       if (!warp_top_k(v, s.E, s.k, lane, pe, pw, rank) && lane == 0) raise_status(A.ctl, kStatusBounds);
+      if (s.bias_sel) pw = warp_pick_weight(warp_logit_of(u, pe), s.k, lane);
       if (lane < s.k) {
         sel_e[t][rank] = pe;
         sel_w[t][rank] = pw;

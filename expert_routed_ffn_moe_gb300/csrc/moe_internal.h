@@ -56,6 +56,7 @@ struct Shapes {
   int T, d, E, I, k;
   int has_shared;
   int x_bf16;             // 1: x is bf16, 0: fp32
+  int bias_sel;           // 1: the router bias picks the experts but does not enter their weights
 };
 
 // moe_route.cu

@@ -193,7 +193,7 @@ __global__ void __launch_bounds__(1024) select_kernel(Shapes s, const float* __r
   __syncthreads();
   const int t = t0 + warp;
   if (t < s.T) {
-    float v[8];
+    float v[8], u[8];  // logits with and without the router bias
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
       const int e = lane + 32 * i;
@@ -206,13 +206,16 @@ __global__ void __launch_bounds__(1024) select_kernel(Shapes s, const float* __r
         } else {
           l = sc.logits[te];
         }
+        u[i] = l;
         if (rb) l += rb[e];
       }
       v[i] = l;
+      if (e >= s.E) u[i] = -INFINITY;
     }
     int pe, rank;
     float pw;
     if (!warp_top_k(v, s.E, s.k, lane, pe, pw, rank) && lane == 0) raise_status(ctl, kStatusBounds);
+    if (s.bias_sel) pw = warp_pick_weight(warp_logit_of(u, pe), s.k, lane);
     if (lane < s.k) {
       sc.idx[(size_t)t * s.k + rank] = pe;
       sc.w[(size_t)t * s.k + rank] = pw;

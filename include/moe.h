@@ -84,6 +84,9 @@ typedef struct moe_config {
   int x_dtype;         /* MOE_F32 or MOE_BF16 */
   int has_router_bias; /* 1: calls pass router_b */
   int has_shared;      /* 1: calls pass shared_w */
+  int bias_select_only; /* 1 (with has_router_bias): router_b takes part in picking the top_k experts
+                           but not in their weights, which are the softmax of the unbiased logits over
+                           the picks (a bias used only to balance expert load); 0: the bias enters both */
 } moe_config;
 
 typedef struct moe_ctx moe_ctx;

@@ -38,10 +38,11 @@ def device_inputs(w: mw.Workload, inp: dict, dev="cuda"):
     )
 
 
-def make_layer(w: mw.Workload, max_tokens=None, path=moe.MOE_PATH_AUTO, router=moe.MOE_ROUTER_AUTO):
+def make_layer(w: mw.Workload, max_tokens=None, path=moe.MOE_PATH_AUTO, router=moe.MOE_ROUTER_AUTO,
+               bias_select_only=False):
     layer = moe.MoeLayer(w.d, w.E, w.I, w.k, max_tokens or w.T,
                          x_dtype=moe.MOE_F32 if w.x_dtype == "f32" else moe.MOE_BF16,
-                         has_router_bias=w.skewed, has_shared=w.I_s > 0)
+                         has_router_bias=w.skewed, has_shared=w.I_s > 0, bias_select_only=bias_select_only)
     moe.moe_set_path(layer.ctx, path)
     moe.moe_set_router(layer.ctx, router)
     return layer
@@ -58,11 +59,13 @@ def gpu_run(w, inp, layer, dev_in=None, top_k=None):
     return {key: v.cpu().numpy() for key, v in r.items()}, y
 
 
-def oracle_routing(w, inp, k=None):
+def oracle_routing(w, inp, k=None, bias_select_only=False):
     k = k or w.k
-    logits = oracle.router_logits(oracle.as_f64(inp["x"], w.x_dtype == "bf16"),
-                                  inp["router_w"].astype(np.float64), inp["router_b"])
-    idx, wts, margin = oracle.route(logits, k)
+    x = oracle.as_f64(inp["x"], w.x_dtype == "bf16")
+    logits = oracle.router_logits(x, inp["router_w"].astype(np.float64), inp["router_b"])
+    unbiased = (oracle.router_logits(x, inp["router_w"].astype(np.float64), None)
+                if bias_select_only and inp["router_b"] is not None else None)
+    idx, wts, margin = oracle.route(logits, k, weight_logits=unbiased)
     counts, offsets, perm, slot = oracle.group(idx, w.E)
     return dict(idx=idx, w=wts, margin=margin, counts=counts, offsets=offsets, perm=perm, slot=slot)
 
@@ -76,11 +79,11 @@ def check_routing(got, ref):
     assert np.all(err <= W_REL * ref["w"] + 1e-7), f"routing weights differ (max {err.max():.3e})"
 
 
-def oracle_y(w, inp, tokens, k=None):
+def oracle_y(w, inp, tokens, k=None, bias_select_only=False):
     """fp64 oracle output rows for `tokens`, drawing only the experts they use."""
     k = k or w.k
     r = oracle.moe_layer(inp["x"], inp["router_w"], inp["router_b"], inp["gate_up"], inp["down"], inp["shared"],
-                         k, x_bf16=w.x_dtype == "bf16", tokens=tokens)
+                         k, x_bf16=w.x_dtype == "bf16", tokens=tokens, bias_select_only=bias_select_only)
     return r["y"]
 
 

@@ -311,3 +311,22 @@ def test_chunked_prefill_matches_oracle_and_unchunked():
     assert torch.equal(y_chunked, y_full)
     toks = sample_tokens(w.T, 48)
     check_y(y_host(y_chunked)[toks], oracle_y(w, inp, toks), "chunked prefill")
+
+
+@pytest.mark.parametrize("T,path", [(1, moe.MOE_PATH_AUTO), (4, moe.MOE_PATH_AUTO), (200, moe.MOE_PATH_AUTO),
+                                    (8, moe.MOE_PATH_GEMM)])
+def test_router_bias_for_selection_only(T, path):
+    # bias_select_only: the Zipf-like bias picks the experts, the weights are
+    # the softmax of the unbiased logits over the picks (fused decode kernel at
+    # T = 1 and 4, grouped GEMMs at T = 200 and T = 8 forced)
+    w = custom(f"biassel{T}", T=T, skewed=True)
+    inp = layer_inputs(w)
+    layer = make_layer(w, path=path, bias_select_only=True)
+    got, y = gpu_run(w, inp, layer)
+    layer.close()
+    check_routing(got, oracle_routing(w, inp, bias_select_only=True))
+    toks = sample_tokens(w.T, 40)
+    check_y(y_host(y)[toks], oracle_y(w, inp, toks, bias_select_only=True), f"bias for selection only, T={T}")
+    # the plain reading differs on these inputs: the bias also scales the weights there
+    ref_plain = oracle_routing(w, inp)
+    assert not np.allclose(got["w"], ref_plain["w"], rtol=1e-3)
