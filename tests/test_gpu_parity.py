@@ -313,7 +313,7 @@ def test_chunked_prefill_matches_oracle_and_unchunked():
     check_y(y_host(y_chunked)[toks], oracle_y(w, inp, toks), "chunked prefill")
 
 
-@pytest.mark.parametrize("T,path", [(1, moe.MOE_PATH_AUTO), (4, moe.MOE_PATH_AUTO), (200, moe.MOE_PATH_AUTO),
+@pytest.mark.parametrize("T,path", [(1, moe.MOE_PATH_AUTO), (4, moe.MOE_PATH_GEMV), (200, moe.MOE_PATH_AUTO),
                                     (8, moe.MOE_PATH_GEMM)])
 def test_router_bias_for_selection_only(T, path):
     # bias_select_only: the Zipf-like bias picks the experts, the weights are
