@@ -12,6 +12,7 @@ from .moe_oracle import (  # noqa: F401
     route,
     router_logits,
     select_top_k,
+    sigmoid,
     silu,
     softmax,
     swiglu_ffn,

@@ -30,6 +30,12 @@ rounded; stored inputs are decoded exactly: fp32 as is, bf16 bits -> float):
 8. output y_t = sum_j w[t, j] * o_{idx[t, j]}(x_t) + o_shared(x_t), summed over
    j in ascending expert order.
 
+Variants the pages do not describe (plain readings, each pinned on its own):
+- bias for selection only: the router bias decides which experts are picked,
+  and the picks' weights are the softmax of the unbiased logits over them.
+- sigmoid-gated shared expert: o_shared(x_t) is scaled by sigmoid(x_t . g) for
+  a gate vector g of d fp32 values (no bias).
+
 Library primitives used as steps: numpy matmul (a dot product per output
 element), ``numpy.exp``, ``numpy.argsort`` (stable) and ``numpy.bincount``.
 
@@ -132,8 +138,15 @@ def swiglu_ffn(x_rows: np.ndarray, gate_up: np.ndarray, down: np.ndarray) -> np.
     return h @ down.T
 
 
+def sigmoid(z: np.ndarray) -> np.ndarray:
+    """sigmoid(z) = 1 / (1 + exp(-z))."""
+    with np.errstate(over="ignore"):
+        return 1.0 / (1.0 + np.exp(-z))
+
+
 def moe_layer(x, router_w, router_b, gate_up, down, shared, k, *, x_bf16: bool,
-              shared_inter: int | None = None, tokens=None, expert_ids=None, bias_select_only: bool = False):
+              shared_inter: int | None = None, tokens=None, expert_ids=None, bias_select_only: bool = False,
+              shared_gate_w=None):
     """Steps 1-8 for the token rows ``tokens`` (default: all).
 
     x        [T, d]  fp32 values, or bf16 bits when ``x_bf16``
@@ -144,6 +157,8 @@ def moe_layer(x, router_w, router_b, gate_up, down, shared, k, *, x_bf16: bool,
              0..n-1); lets a caller pass only the experts the sampled tokens use.
     bias_select_only  the router bias picks the experts but their weights are
              the softmax of the unbiased logits over the picks.
+    shared_gate_w  [d] fp32 gate vector, or None: the shared expert's output
+             is scaled by sigmoid(x_t . shared_gate_w).
 
     Returns dict(y [n_tok, d] fp64, idx, w, margin, logits) for those tokens."""
     xs = as_f64(x, x_bf16)
@@ -169,5 +184,8 @@ def moe_layer(x, router_w, router_b, gate_up, down, shared, k, *, x_bf16: bool,
     if shared is not None:
         i_s = shared_inter if shared_inter is not None else len(shared) // (3 * d)
         sh = decode_bf16(shared)
-        y += swiglu_ffn(xs, sh[: 2 * i_s * d].reshape(2 * i_s, d), sh[2 * i_s * d:].reshape(d, i_s))
+        o_s = swiglu_ffn(xs, sh[: 2 * i_s * d].reshape(2 * i_s, d), sh[2 * i_s * d:].reshape(d, i_s))
+        if shared_gate_w is not None:
+            o_s = sigmoid(xs @ np.asarray(shared_gate_w, dtype=np.float64))[:, None] * o_s
+        y += o_s
     return dict(y=y, idx=idx, w=w, margin=margin, logits=logits)

@@ -370,6 +370,47 @@ def test_layer_shared_and_routed_parts_separate():
     assert np.all(oracle.moe_layer(x, wr, None, gu, dn, np.zeros_like(sh), 2, x_bf16=False)["y"] == routed)
 
 
+def test_sigmoid_closed_forms():
+    z = np.array([0.0, math.log(3.0), -math.log(3.0), 40.0, -40.0, -800.0])
+    got = oracle.sigmoid(z)
+    assert got[0] == 0.5
+    assert abs(got[1] - 0.75) < 1e-15 and abs(got[2] - 0.25) < 1e-15
+    assert got[3] == 1.0 and 0.0 < got[4] < 1e-17 and got[5] == 0.0
+    r = np.random.default_rng(3).normal(size=50) * 5
+    assert np.allclose(oracle.sigmoid(r) + oracle.sigmoid(-r), 1.0, atol=1e-15, rtol=0)
+    assert np.allclose(oracle.sigmoid(r), scipy.special.expit(r), atol=1e-16, rtol=1e-15)
+
+
+def test_shared_gate_scales_only_the_shared_expert():
+    # g = the first unit vector, so token t's gate logit is x[t, 0]: gates of
+    # exactly 1/2, 3/4, 1/4, ~1 and ~0 (sigmoid(ln 3) = 1 / (1 + 1/3) = 3/4).
+    rng = np.random.default_rng(12)
+    x, wr, gu, dn, sh = tiny_layer(rng, T=5, E=4, d=8, inter=4, k=2)
+    x = x.astype(np.float64)
+    x[:, 0] = [0.0, math.log(3.0), -math.log(3.0), 40.0, -40.0]
+    g = np.zeros(8)
+    g[0] = 1.0
+    want_gate = np.array([0.5, 0.75, 0.25, 1.0, 0.0])
+    gated = oracle.moe_layer(x, wr, None, gu, dn, sh, 2, x_bf16=False, shared_gate_w=g)
+    plain = oracle.moe_layer(x, wr, None, gu, dn, sh, 2, x_bf16=False)
+    routed = oracle.moe_layer(x, wr, None, gu, dn, None, 2, x_bf16=False)["y"]
+    # the gate changes neither the picks nor their weights
+    assert np.array_equal(gated["idx"], plain["idx"]) and np.array_equal(gated["w"], plain["w"])
+    shared_part = plain["y"] - routed
+    assert np.all(np.abs(shared_part).max(axis=1) > 1e-3)
+    assert np.allclose(gated["y"], routed + want_gate[:, None] * shared_part, atol=1e-12, rtol=0)
+    # without a shared expert the gate vector is ignored
+    r = oracle.moe_layer(x, wr, None, gu, dn, None, 2, x_bf16=False, shared_gate_w=g)["y"]
+    assert np.array_equal(r, routed)
+    # a general gate vector: the logit is the dot product with the token row
+    g2 = rng.normal(size=8)
+    gated2 = oracle.moe_layer(x[:3], wr, None, gu, dn, sh, 2, x_bf16=False, shared_gate_w=g2)["y"]
+    for t in range(3):
+        z = sum(float(x[t, i]) * float(g2[i]) for i in range(8))
+        s_t = 1.0 / (1.0 + math.exp(-z))
+        assert np.allclose(gated2[t], routed[t] + s_t * shared_part[t], atol=1e-12, rtol=0)
+
+
 def test_layer_token_permutation_equivariance_and_subsets():
     rng = np.random.default_rng(11)
     x, wr, gu, dn, sh = tiny_layer(rng, T=11, E=7, d=8, inter=4, k=3)
