@@ -161,8 +161,10 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------------ inputs
-def device_weights(w: mw.Workload, layer: int, dev):
-    """Seeded device-side weights of one layer (torch CUDA generator)."""
+def device_weights(w: mw.Workload, layer: int, dev, shared_gate=False):
+    """Seeded device-side weights of one layer (torch CUDA generator).  With
+    ``shared_gate`` the router gets a row E: the gate vector of a sigmoid-gated
+    shared expert, ~ N(0, 0.9^2 / d) like ``moe_workloads.draw_shared_gate``."""
     import torch
 
     g = torch.Generator(device=dev)
@@ -178,6 +180,9 @@ def device_weights(w: mw.Workload, layer: int, dev):
         return out
 
     router_w = torch.randn(w.E, w.d, generator=g, device=dev) * 0.02
+    if shared_gate:
+        gate = torch.randn(1, w.d, generator=g, device=dev) * (0.9 / w.d ** 0.5)
+        router_w = torch.cat([router_w, gate])
     router_b = None
     if w.skewed:
         router_b = torch.tensor(mw.draw_router(w, layer)[1], device=dev)
@@ -195,8 +200,9 @@ def host_x(w: mw.Workload, layer: int):
 
 
 # ------------------------------------------------------------------ algorithmic bytes / flops
-def layer_costs(w: mw.Workload, idx: np.ndarray):
-    """Bytes and flops a layer must move/compute, from its actual routing."""
+def layer_costs(w: mw.Workload, idx: np.ndarray, shared_gate=False):
+    """Bytes and flops a layer must move/compute, from its actual routing
+    (with ``shared_gate``, the router's extra gate row as well)."""
     distinct = len(np.unique(idx)) + (1 if w.I_s else 0)
     expert_bytes = 3 * w.d * w.I * 2
     xb = 2 if w.x_dtype == "bf16" else 4
@@ -204,7 +210,7 @@ def layer_costs(w: mw.Workload, idx: np.ndarray):
     return dict(
         distinct=distinct,
         gate_up_bytes=distinct * 2 * w.I * w.d * 2 + w.T * w.d * xb,
-        layer_bytes=distinct * expert_bytes + w.E * w.d * 4 + 2 * w.T * w.d * xb,
+        layer_bytes=distinct * expert_bytes + (w.E + int(shared_gate)) * w.d * 4 + 2 * w.T * w.d * xb,
         gate_up_flops=2.0 * rows * w.d * 2 * w.I,
         layer_flops=2.0 * rows * 3 * w.d * w.I,
     )
@@ -232,7 +238,8 @@ def oracle_sample(w: mw.Workload, budget_s: float, host_inputs):
     while True:
         for inp in host_inputs:
             oracle.moe_layer(inp["x"], inp["router_w"], inp["router_b"], inp["gate_up"], inp["down"], inp["shared"],
-                             w.k, x_bf16=w.x_dtype == "bf16", tokens=inp["tokens"], expert_ids=inp["expert_ids"])
+                             w.k, x_bf16=w.x_dtype == "bf16", tokens=inp["tokens"], expert_ids=inp["expert_ids"],
+                             shared_gate_w=inp.get("shared_gate_w"))
             done += len(inp["tokens"])
         el = time.perf_counter() - t0
         if el >= budget_s:
@@ -250,7 +257,8 @@ def host_layer_for_oracle(w, layer, dev_w, x_host, n_tokens=8, seed=0):
         return t.contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
 
     x = x_host.numpy() if w.x_dtype == "f32" else bits(x_host)
-    wr = dev_w["router_w"].cpu().numpy()
+    wr_all = dev_w["router_w"].cpu().numpy()
+    wr, gate = wr_all[:w.E], (wr_all[w.E] if wr_all.shape[0] > w.E else None)
     rb = None if dev_w["router_b"] is None else dev_w["router_b"].cpu().numpy()
     rng = np.random.default_rng(seed + layer)
     toks = np.sort(rng.choice(w.T, min(w.T, n_tokens), replace=False))
@@ -258,7 +266,8 @@ def host_layer_for_oracle(w, layer, dev_w, x_host, n_tokens=8, seed=0):
     used = np.unique(oracle.route(logits, w.k)[0])
     return dict(x=x, router_w=wr, router_b=rb, gate_up=bits(dev_w["gate_up"][torch.from_numpy(used).to(
         dev_w["gate_up"].device)]), down=bits(dev_w["down"][torch.from_numpy(used).to(dev_w["down"].device)]),
-        shared=None if dev_w["shared"] is None else bits(dev_w["shared"]), expert_ids=used, tokens=toks)
+        shared=None if dev_w["shared"] is None else bits(dev_w["shared"]), expert_ids=used, tokens=toks,
+        shared_gate_w=gate)
 
 
 # ------------------------------------------------------------------ multi-rank bookkeeping
@@ -297,7 +306,7 @@ def run_ours(args, rank, world, dev):
     torch.cuda.set_device(dev)
     stream = torch.cuda.Stream(device=dev)
 
-    weights = [device_weights(w, L, dev) for L in range(layers)]
+    weights = [device_weights(w, L, dev, args.shared_gate) for L in range(layers)]
     # one pinned host block and one device block for all layers' tokens, so an
     # end-to-end step moves its inputs and results in one copy each way
     xh_all = torch.stack([host_x(w, replica_layer(L, rank)) for L in range(layers)]).pin_memory()
@@ -307,7 +316,7 @@ def run_ours(args, rank, world, dev):
     xh, xd, yd, yh = list(xh_all), list(xd_all), list(yd_all), list(yh_all)
     max_tokens = args.chunk if args.chunk else w.T
     ctx = moe.MoeLayer(w.d, w.E, w.I, w.k, max_tokens, x_dtype=moe.MOE_F32 if w.x_dtype == "f32" else moe.MOE_BF16,
-                       has_router_bias=w.skewed, has_shared=w.I_s > 0)
+                       has_router_bias=w.skewed, has_shared=w.I_s > 0, shared_gate=args.shared_gate)
     if args.chunk:  # chunked prefill: workspace for `chunk` tokens, the layer over all T in slices
         moe.moe_set_chunk_tokens(ctx.ctx, args.chunk)
     path = moe.MOE_PATH_AUTO if args.path == "auto" else (moe.MOE_PATH_GEMV if args.path == "gemv"
@@ -351,7 +360,7 @@ def run_ours(args, rank, world, dev):
             step_t = args.chunk or w.T  # moe_route keeps the T <= max_tokens limit: route slice by slice
             idx = [ctx.route(xd[L][t0:t0 + step_t], p["router_w"], p["router_b"], stream=stream)["idx"].cpu().numpy()
                    for t0 in range(0, w.T, step_t)]
-            costs.append(layer_costs(w, np.concatenate(idx)))
+            costs.append(layer_costs(w, np.concatenate(idx), args.shared_gate))
         for _ in range(max(args.warmup, 0)):
             step()
     stream.synchronize()
@@ -488,7 +497,8 @@ def run_ours(args, rank, world, dev):
                                    if layer_bytes * layers > L2_BYTES else
                                    f"inputs fit in L2 ({layer_bytes * layers / 1e6:.0f} MB per step): "
                                    f"a profiling run, not a bench number"),
-                               parallelism=f"replicas x{world}", **({"chunk_tokens": args.chunk} if args.chunk else {})),
+                               parallelism=f"replicas x{world}", **({"chunk_tokens": args.chunk} if args.chunk else {}),
+                               **({"shared_gate": "sigmoid"} if args.shared_gate else {})),
                    e2e=dict(value=round(e2e_value, 1), unit=UNIT,
                             h2d_bytes_per_step=int(sum(t.numel() * t.element_size() for t in xh)),
                             d2h_bytes_per_step=int(sum(t.numel() * t.element_size() for t in yh))),
@@ -546,6 +556,8 @@ def main():
                     help="chunked prefill: size the workspace for this many tokens and run T in slices")
     ap.add_argument("--layers", type=int, default=0,
                     help="stacked layers per step (default: the workload's own; fewer only for small profiling runs)")
+    ap.add_argument("--shared-gate", action="store_true",
+                    help="the sigmoid-gated shared-expert variant (a gate row appended to the router)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 

@@ -33,7 +33,8 @@ class MoeError(RuntimeError):
 
 class moe_config(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int) for n in ("d", "n_experts", "inter", "shared_inter", "top_k", "max_tokens",
-                                            "x_dtype", "has_router_bias", "has_shared", "bias_select_only")]
+                                            "x_dtype", "has_router_bias", "has_shared", "bias_select_only",
+                                            "shared_gate")]
 
 
 _lib = None
@@ -119,9 +120,9 @@ def moe_strerror(code: int) -> str:
 
 
 def moe_init(d, n_experts, inter, shared_inter, top_k, max_tokens, x_dtype=MOE_BF16, has_router_bias=False,
-             has_shared=True, bias_select_only=False) -> ctypes.c_void_p:
+             has_shared=True, bias_select_only=False, shared_gate=False) -> ctypes.c_void_p:
     cfg = moe_config(d, n_experts, inter, shared_inter, top_k, max_tokens, x_dtype, int(has_router_bias),
-                     int(has_shared), int(bias_select_only))
+                     int(has_shared), int(bias_select_only), int(shared_gate))
     h = ctypes.c_void_p()
     _check(lib().moe_init(ctypes.byref(cfg), ctypes.byref(h)), "moe_init")
     return h
@@ -232,12 +233,15 @@ class MoeLayer:
     """Owns one context; ``forward`` / ``route`` call the C ABI on torch tensors."""
 
     def __init__(self, d, n_experts, inter, top_k, max_tokens, *, shared_inter=None, x_dtype=MOE_BF16,
-                 has_router_bias=False, has_shared=True, bias_select_only=False):
+                 has_router_bias=False, has_shared=True, bias_select_only=False, shared_gate=False):
+        """``shared_gate``: sigmoid-gated shared expert; router_w then holds n_experts + 1
+        rows, the last being the gate vector."""
         self.top_k = top_k
         self.d = d
+        self.n_experts = n_experts
         self.x_dtype = x_dtype
         self.ctx = moe_init(d, n_experts, inter, inter if shared_inter is None else shared_inter, top_k,
-                            max_tokens, x_dtype, has_router_bias, has_shared, bias_select_only)
+                            max_tokens, x_dtype, has_router_bias, has_shared, bias_select_only, shared_gate)
 
     def forward(self, x, router_w, router_b, gate_up, down, shared_w, y=None, top_k=None, stream=None):
         import torch
@@ -252,7 +256,7 @@ class MoeLayer:
 
         k = top_k or self.top_k
         T = x.shape[0]
-        E = router_w.shape[0]
+        E = self.n_experts
         dev = x.device
         out = dict(idx=torch.empty(T, k, dtype=torch.int32, device=dev),
                    w=torch.empty(T, k, dtype=torch.float32, device=dev),

@@ -98,6 +98,7 @@ Shapes shapes(const moe_ctx* ctx, int T, int top_k) {
   s.has_shared = c.has_shared;
   s.x_bf16 = c.x_dtype == MOE_BF16;
   s.bias_sel = c.has_router_bias && c.bias_select_only;
+  s.shared_gate = c.has_shared && c.shared_gate;
   return s;
 }
 
@@ -162,7 +163,8 @@ int run_route(moe_ctx* ctx, const Shapes& s, const void* x, const float* wr, con
     err = launch(ctx, MOE_K_ROUTER, st, [&] { return launch_router_logits_simt(s, x, wr, rb, sc, st); });
     if (err != cudaSuccess) return cuda_fail(err);
   }
-  err = launch(ctx, MOE_K_SELECT, st, [&] { return launch_select(s, rb, parts, sc, ctl, st); });
+  const float* gate_w = s.shared_gate ? wr + (size_t)s.E * s.d : nullptr;  // router row E
+  err = launch(ctx, MOE_K_SELECT, st, [&] { return launch_select(s, rb, parts, sc, ctl, st, x, gate_w); });
   if (err != cudaSuccess) return cuda_fail(err);
   err = launch(ctx, MOE_K_GROUP, st, [&] { return launch_group(s, sc, ctl, st, permute_rows ? x : nullptr); });
   ctx->launches += 1;  // the group step is two kernels
@@ -197,6 +199,8 @@ int moe_init(const moe_config* cfg, moe_ctx** out) {
   if (c.n_experts > kMaxExperts || c.d % 256 != 0 || c.inter % 128 != 0) return MOE_ERR_UNSUPPORTED;
   if (c.has_shared && c.shared_inter != c.inter) return MOE_ERR_UNSUPPORTED;
   if (c.bias_select_only != 0 && c.bias_select_only != 1) return MOE_ERR_ARG;
+  if (c.shared_gate != 0 && c.shared_gate != 1) return MOE_ERR_ARG;
+  if (c.shared_gate && !c.has_shared) return MOE_ERR_ARG;
   if ((long long)c.max_tokens * (c.top_k + 1) >= (1LL << 31) / 2) return MOE_ERR_UNSUPPORTED;
 
   int dev = 0;
@@ -227,6 +231,7 @@ int moe_init(const moe_config* cfg, moe_ctx** out) {
     s1.k = c.top_k;
     s1.has_shared = c.has_shared;
     s1.x_bf16 = c.x_dtype == MOE_BF16;
+    s1.shared_gate = c.has_shared && c.shared_gate;
     if (decode_supported(s1, kDecodeSmemLimit) && decode_blocks_per_sm(s1, kDecodeSmemLimit) >= 1) ctx->decode_max_t = t;
   }
 
@@ -275,6 +280,7 @@ int moe_init(const moe_config* cfg, moe_ctx** out) {
   const size_t o_dlog = take(ctx->decode_max_t ? (size_t)kDecodeReps * ctx->decode_max_t * E * 8 : 16);
   const size_t dpairs = (size_t)ctx->decode_max_t * (k + 1);
   const size_t o_dh = take(ctx->decode_max_t ? (size_t)kDecodeReps * dpairs * I * 8 : 16);
+  const size_t o_sgate = take(T * 4);
   if (cudaMalloc(&ctx->block, off) != cudaSuccess) {
     cudaGetLastError();
     delete ctx;
@@ -309,6 +315,7 @@ int moe_init(const moe_config* cfg, moe_ctx** out) {
   sc.gridbar = reinterpret_cast<unsigned*>(b + o_gridbar);
   sc.dec_logits = reinterpret_cast<float*>(b + o_dlog);
   sc.dec_h = reinterpret_cast<float*>(b + o_dh);
+  sc.sgate = reinterpret_cast<float*>(b + o_sgate);
   sc.dec_reps = kDecodeReps;
   sc.dec_hreps = kDecodeReps;
   sc.max_mtiles = max_mtiles;

@@ -3,8 +3,9 @@
 // "Optimizing on-device inference for Apple Silicon", section "Reducing
 // intermediate and state traffic": the experts' output projections are
 // combined with their routing scores and the shared expert's result.  Here,
-// per token t: y_t = sum_j w[t, j] * out[slot[t, j]] + out[T*k + t], summed in
-// fp32 over j in ascending expert order, then stored in x's dtype.
+// per token t: y_t = sum_j w[t, j] * out[slot[t, j]] + g_t * out[T*k + t],
+// summed in fp32 over j in ascending expert order, then stored in x's dtype;
+// g_t is one, or sigmoid(x_t . g) for a sigmoid-gated shared expert.
 #include "moe_internal.h"
 
 namespace moe {
@@ -34,15 +35,17 @@ __global__ void __launch_bounds__(256) combine_kernel(Shapes s, void* __restrict
     acc[7] = fmaf(wj, bf16_hi(v.w), acc[7]);
   }
   if (s.has_shared) {
+    // fmaf with a gate of exactly one adds v exactly as a plain sum would
+    const float gs = s.shared_gate ? sc.sgate[t] : 1.f;
     const uint4 v = __ldcs(reinterpret_cast<const uint4*>(sc.out + ((size_t)s.T * s.k + t) * s.d + col));
-    acc[0] += bf16_lo(v.x);
-    acc[1] += bf16_hi(v.x);
-    acc[2] += bf16_lo(v.y);
-    acc[3] += bf16_hi(v.y);
-    acc[4] += bf16_lo(v.z);
-    acc[5] += bf16_hi(v.z);
-    acc[6] += bf16_lo(v.w);
-    acc[7] += bf16_hi(v.w);
+    acc[0] = fmaf(gs, bf16_lo(v.x), acc[0]);
+    acc[1] = fmaf(gs, bf16_hi(v.x), acc[1]);
+    acc[2] = fmaf(gs, bf16_lo(v.y), acc[2]);
+    acc[3] = fmaf(gs, bf16_hi(v.y), acc[3]);
+    acc[4] = fmaf(gs, bf16_lo(v.z), acc[4]);
+    acc[5] = fmaf(gs, bf16_hi(v.z), acc[5]);
+    acc[6] = fmaf(gs, bf16_lo(v.w), acc[6]);
+    acc[7] = fmaf(gs, bf16_hi(v.w), acc[7]);
   }
   if (YBF16) {
     uint4 o = make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]), pack_bf16x2(acc[4], acc[5]),

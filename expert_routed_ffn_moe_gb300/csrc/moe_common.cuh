@@ -42,6 +42,7 @@ MOE_DEV float warp_sum(float v) {
   return v;
 }
 MOE_DEV float silu(float g) { return g / (1.0f + __expf(-g)); }
+MOE_DEV float sigmoid(float z) { return 1.0f / (1.0f + __expf(-z)); }
 
 // ---------------------------------------------------------------- top-k selection
 // Order-preserving map of an fp32 value to u32 (NaN taken as -inf).

@@ -29,7 +29,9 @@
 //   phase C  one warp per output feature: for the active experts in ascending
 //            id (shared expert last) the down-projection row, dotted with each
 //            routed token's h, scaled by its routing weight, summed per token
-//            in fp32 and written to y.
+//            in fp32 and written to y.  The shared expert's weight is one,
+//            or sigmoid(x_t . g) for a sigmoid-gated shared expert (g = router
+//            row E; each block computes it beside its selection).
 // h is written in several copies and block b reads copy b mod copies, so that
 // no L2 line is read by every SM at once.
 //
@@ -250,6 +252,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const DecodeA
   __shared__ unsigned act_m[kMaxExperts + 1];
   __shared__ int act_row[kMaxExperts + 1];      // first grouped h row of each active expert
   __shared__ float act_w[kMaxExperts + 1][MAXT];
+  __shared__ float sgate_s[MAXT];               // the shared expert's weight per token
   __shared__ int n_act_s, flag_s;
   __shared__ unsigned ep_s;  // this launch's epoch: the tag of every value it publishes
   __shared__ int warp_tot[kWarps];
@@ -291,9 +294,11 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const DecodeA
     }
     // this block's shared-expert neurons i = b + q G (items q < n_sh of the
     // weight stream) start streaming into the ring now: they need no routing
-    if (tid == 0)
+    if (tid == 0) {
       for (int q = 0; q < n_sh && q < A.ring_slots; ++q)
         issue_item(A, q, q, n_sh, 0, 1, b, G, 0, nullptr, ring, full, slot_issued);
+      if (s.shared_gate) prefetch_l2(A.wr + (size_t)s.E * s.d, (uint32_t)s.d * 4u);  // the gate row, for phase B
+    }
     // Everything above reads weights only.  Launched with programmatic stream
     // serialization, this block may have started while the previous kernel
     // on the stream is still running: wait for it before touching x or any
@@ -396,6 +401,23 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const DecodeA
     // test hook: wait for a tag that no block writes
     const unsigned want = ep_s + (A.ctl.stall ? 1u : 0u);
     for (int t = warp; t < s.T; t += kWarps) {
+      // the shared expert's weight: one, or sigmoid(x_t . g) for the gate
+      // vector g in router row E (computed while other blocks finish routing)
+      float sg = 1.f;
+      if (s.shared_gate) {
+        const float4* g4 = reinterpret_cast<const float4*>(A.wr + (size_t)s.E * s.d);
+        const float4* xr = reinterpret_cast<const float4*>(big + (size_t)t * s.d);
+        float acc = 0.f;
+        for (int c = lane; c < s.d / 4; c += 32) {
+          const float4 gv = __ldg(g4 + c), xv = xr[c];
+          acc = fmaf(xv.x, gv.x, acc);
+          acc = fmaf(xv.y, gv.y, acc);
+          acc = fmaf(xv.z, gv.z, acc);
+          acc = fmaf(xv.w, gv.w, acc);
+        }
+        sg = sigmoid(warp_sum(acc));
+      }
+      if (lane == 0) sgate_s[t] = sg;
       float v[8], u[8];  // logits with and without the router bias
 #pragma unroll
       for (int i = 0; i < 8; ++i) v[i] = (A.rb && lane + 32 * i < s.E) ? __ldg(A.rb + lane + 32 * i) : 0.f;
@@ -456,7 +478,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const DecodeA
           act_e[s.k] = s.E;
           act_m[s.k] = 1u;
           act_row[s.k] = s.k;
-          act_w[s.k][0] = 1.f;
+          act_w[s.k][0] = sg;
         }
         n_act_s = s.k + (s.has_shared ? 1 : 0);
       }
@@ -507,7 +529,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const DecodeA
           act_e[n_routed] = s.E;
           act_m[n_routed] = (s.T >= 32) ? 0xffffffffu : ((1u << s.T) - 1u);
           act_row[n_routed] = tk;
-          for (int t = 0; t < MAXT; ++t) act_w[n_routed][t] = t < s.T ? 1.f : 0.f;
+          for (int t = 0; t < MAXT; ++t) act_w[n_routed][t] = t < s.T ? sgate_s[t] : 0.f;
         }
         n_act_s = n_routed + (s.has_shared ? 1 : 0);
       }
@@ -625,7 +647,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const DecodeA
     // pull them into L2 while this phase is bound by latency, not bandwidth
     // (the last warp: it has no output row when d < kWarps G)
     if (warp == kWarps - 1) {
-      const size_t rbytes = (size_t)s.E * s.d * 4, sbytes = (size_t)3 * s.I * s.d * 2;
+      const size_t rbytes = (size_t)(s.E + s.shared_gate) * s.d * 4, sbytes = (size_t)3 * s.I * s.d * 2;
       const size_t rper = ((rbytes / G) + 4095) & ~size_t(4095), sper = ((sbytes / G) + 4095) & ~size_t(4095);
       if (A.next_wr)
         for (size_t off = rper * b + (size_t)lane * 4096; off < min(rbytes, rper * (b + 1)); off += 32 * 4096)

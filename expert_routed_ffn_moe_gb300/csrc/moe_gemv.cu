@@ -137,7 +137,7 @@ __global__ void __launch_bounds__(kGemvWarps * 32) gemv_down_kernel(Shapes s, co
     pt[p] = q / s.k;
   }
   for (int t = threadIdx.x; t < n_pairs - tk; t += blockDim.x) {
-    pw[tk + t] = 1.f;
+    pw[tk + t] = s.shared_gate ? sc.sgate[t] : 1.f;
     pt[tk + t] = t;
   }
   __syncthreads();

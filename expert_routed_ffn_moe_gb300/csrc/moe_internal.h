@@ -50,6 +50,7 @@ struct Scratch {
   unsigned* gridbar;      // fused decode kernel: [1] epoch of the last launch
   float* dec_logits;      // fused decode kernel: [dec_reps][T][E] router logits as (fp32, epoch) 64-bit words
   float* dec_h;           // fused decode kernel: [dec_hreps][T*k + T][I] SwiGLU activations as (fp32, epoch) words
+  float* sgate;           // [T] sigmoid(x_t . g), the shared expert's gate (GEMV and GEMM paths)
   int dec_reps;           // copies of the logits (blocks read copy b % reps)
   int dec_hreps;          // copies of h
   int max_mtiles;
@@ -60,14 +61,17 @@ struct Shapes {
   int has_shared;
   int x_bf16;             // 1: x is bf16, 0: fp32
   int bias_sel;           // 1: the router bias picks the experts but does not enter their weights
+  int shared_gate;        // 1: the shared expert's output is scaled by sigmoid(x . g), g = router row E
 };
 
 // moe_route.cu
 cudaError_t launch_router_logits_simt(const Shapes& s, const void* x, const float* wr, const float* rb,
                                       const Scratch& sc, cudaStream_t st);
 cudaError_t launch_router_split_weights(const Shapes& s, const float* wr, const Scratch& sc, cudaStream_t st);
+// with s.shared_gate, also sc.sgate[t] = sigmoid(x_t . gate_w)
 cudaError_t launch_select(const Shapes& s, const float* rb, int logit_parts, const Scratch& sc,
-                          const DevCtl& ctl, cudaStream_t st);
+                          const DevCtl& ctl, cudaStream_t st, const void* x = nullptr,
+                          const float* gate_w = nullptr);
 // x_rows non-null: also write every token's row, in bf16, to its grouped rows of sc.x_perm
 cudaError_t launch_group(const Shapes& s, const Scratch& sc, const DevCtl& ctl, cudaStream_t st,
                          const void* x_rows = nullptr);

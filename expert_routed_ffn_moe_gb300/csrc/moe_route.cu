@@ -182,9 +182,11 @@ cudaError_t launch_router_split_weights(const Shapes& s, const float* wr, const 
 // lane holds 8 logits; k rounds of warp reductions, ties to the lower expert
 // id).  The weights are the softmax over all E experts renormalised over the
 // picks; the picks are written in ascending expert id, and the chunk's
-// per-expert token masks feed the grouping.
+// per-expert token masks feed the grouping.  For a sigmoid-gated shared
+// expert the warp also writes the token's gate, sigmoid(x_t . gate_w).
 __global__ void __launch_bounds__(1024) select_kernel(Shapes s, const float* __restrict__ rb, int parts, Scratch sc,
-                                                      DevCtl ctl) {
+                                                      DevCtl ctl, const void* __restrict__ x,
+                                                      const float* __restrict__ gate_w) {
   __shared__ unsigned mask[kMaxExperts];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int c = blockIdx.x, t0 = c * kChunk;
@@ -221,6 +223,26 @@ __global__ void __launch_bounds__(1024) select_kernel(Shapes s, const float* __r
       sc.w[(size_t)t * s.k + rank] = pw;
       atomicOr(&mask[pe], 1u << warp);
     }
+    if (s.shared_gate) {
+      const float4* g4 = reinterpret_cast<const float4*>(gate_w);
+      float acc = 0.f;
+      for (int c = lane; c < s.d / 4; c += 32) {
+        float4 xv;
+        if (s.x_bf16) {
+          const uint2 raw = __ldg(reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(x) + (size_t)t * s.d) + c);
+          xv = make_float4(bf16_lo(raw.x), bf16_hi(raw.x), bf16_lo(raw.y), bf16_hi(raw.y));
+        } else {
+          xv = __ldg(reinterpret_cast<const float4*>(static_cast<const float*>(x) + (size_t)t * s.d) + c);
+        }
+        const float4 gv = __ldg(g4 + c);
+        acc = fmaf(xv.x, gv.x, acc);
+        acc = fmaf(xv.y, gv.y, acc);
+        acc = fmaf(xv.z, gv.z, acc);
+        acc = fmaf(xv.w, gv.w, acc);
+      }
+      acc = warp_sum(acc);
+      if (lane == 0) sc.sgate[t] = sigmoid(acc);
+    }
   }
   __syncthreads();
   for (int e = tid; e < s.E; e += blockDim.x) {
@@ -231,9 +253,10 @@ __global__ void __launch_bounds__(1024) select_kernel(Shapes s, const float* __r
 }
 
 cudaError_t launch_select(const Shapes& s, const float* rb, int parts, const Scratch& sc, const DevCtl& ctl,
-                          cudaStream_t st) {
+                          cudaStream_t st, const void* x, const float* gate_w) {
+  if (s.shared_gate && (!x || !gate_w)) return cudaErrorInvalidValue;
   const int nchunk = (s.T + kChunk - 1) / kChunk;
-  select_kernel<<<nchunk, kChunk * 32, 0, st>>>(s, rb, parts, sc, ctl);
+  select_kernel<<<nchunk, kChunk * 32, 0, st>>>(s, rb, parts, sc, ctl, x, gate_w);
   return cudaGetLastError();
 }
 

@@ -87,6 +87,9 @@ typedef struct moe_config {
   int bias_select_only; /* 1 (with has_router_bias): router_b takes part in picking the top_k experts
                            but not in their weights, which are the softmax of the unbiased logits over
                            the picks (a bias used only to balance expert load); 0: the bias enters both */
+  int shared_gate;     /* 1 (with has_shared): sigmoid-gated shared expert -- router_w holds E + 1 rows,
+                          row E being a gate vector g of d fp32 values, and the shared expert's output
+                          for token t is scaled by sigmoid(x_t . g) (no bias); 0: weight one */
 } moe_config;
 
 typedef struct moe_ctx moe_ctx;
@@ -112,7 +115,7 @@ int moe_route(moe_ctx* ctx, const void* x, int T, const float* router_w, const f
               void* stream);
 
 /* The whole layer: y [T, d] (cfg->x_dtype) from x [T, d] (cfg->x_dtype),
- * router_w [E, d] fp32, router_b [E] fp32 or NULL, experts_gate_up [E, 2I, d]
+ * router_w [E, d] fp32 ([E + 1, d] with cfg->shared_gate), router_b [E] fp32 or NULL, experts_gate_up [E, 2I, d]
  * bf16 (per expert: rows 0..I-1 gate projection, rows I..2I-1 up projection),
  * experts_down [E, d, I] bf16, shared_w (NULL unless cfg->has_shared): one bf16
  * buffer holding the shared expert's gate_up [2I, d] followed by its down

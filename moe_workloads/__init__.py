@@ -21,6 +21,9 @@ each tensor from its own ``SeedSequence``):
   ``gate_up`` [E, 2I, d] (rows 0..I-1 gate, I..2I-1 up), ``down`` [E, d, I];
 * shared expert    same distribution, one flat bf16 buffer holding its
   gate_up [2I_s, d] followed by its down [d, I_s].
+* shared gate      (the sigmoid-gated shared-expert variant) g ~ N(0, 0.9^2 / d),
+  fp32 [d]: with x ~ N(0, 1) the gate logit x . g has a spread of about 0.9,
+  so the gates cover most of (0, 1).
 
 Each expert is drawn from its own stream, so a caller that needs only a few
 experts (the oracle on a sample of tokens) can draw just those.
@@ -43,7 +46,7 @@ import numpy as np
 SEED_BASE = 20261202
 
 # tensor-kind tags for SeedSequence keys
-_X, _X_REDRAW, _ROUTER_W, _GATE_UP, _DOWN, _SHARED = range(6)
+_X, _X_REDRAW, _ROUTER_W, _GATE_UP, _DOWN, _SHARED, _SHARED_GATE = range(7)
 
 
 @dataclasses.dataclass(frozen=True)
@@ -153,6 +156,11 @@ def draw_shared(w: Workload, layer: int = 0) -> Optional[np.ndarray]:
         return None
     a = _normal(0.02, 3 * w.I_s * w.d, w.seed, layer, _SHARED)
     return f32_to_bf16_bits(a)
+
+
+def draw_shared_gate(w: Workload, layer: int = 0) -> np.ndarray:
+    """Gate vector of the sigmoid-gated shared-expert variant, fp32 [d]."""
+    return _normal(0.9 / math.sqrt(w.d), w.d, w.seed, layer, _SHARED_GATE)
 
 
 def split_shared(w: Workload, shared: np.ndarray):

@@ -39,10 +39,11 @@ def device_inputs(w: mw.Workload, inp: dict, dev="cuda"):
 
 
 def make_layer(w: mw.Workload, max_tokens=None, path=moe.MOE_PATH_AUTO, router=moe.MOE_ROUTER_AUTO,
-               bias_select_only=False):
+               bias_select_only=False, shared_gate=False):
     layer = moe.MoeLayer(w.d, w.E, w.I, w.k, max_tokens or w.T,
                          x_dtype=moe.MOE_F32 if w.x_dtype == "f32" else moe.MOE_BF16,
-                         has_router_bias=w.skewed, has_shared=w.I_s > 0, bias_select_only=bias_select_only)
+                         has_router_bias=w.skewed, has_shared=w.I_s > 0, bias_select_only=bias_select_only,
+                         shared_gate=shared_gate)
     moe.moe_set_path(layer.ctx, path)
     moe.moe_set_router(layer.ctx, router)
     return layer
@@ -79,11 +80,12 @@ def check_routing(got, ref):
     assert np.all(err <= W_REL * ref["w"] + 1e-7), f"routing weights differ (max {err.max():.3e})"
 
 
-def oracle_y(w, inp, tokens, k=None, bias_select_only=False):
+def oracle_y(w, inp, tokens, k=None, bias_select_only=False, shared_gate_w=None):
     """fp64 oracle output rows for `tokens`, drawing only the experts they use."""
     k = k or w.k
     r = oracle.moe_layer(inp["x"], inp["router_w"], inp["router_b"], inp["gate_up"], inp["down"], inp["shared"],
-                         k, x_bf16=w.x_dtype == "bf16", tokens=tokens, bias_select_only=bias_select_only)
+                         k, x_bf16=w.x_dtype == "bf16", tokens=tokens, bias_select_only=bias_select_only,
+                         shared_gate_w=shared_gate_w)
     return r["y"]
 
 

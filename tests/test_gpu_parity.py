@@ -330,3 +330,33 @@ def test_router_bias_for_selection_only(T, path):
     # the plain reading differs on these inputs: the bias also scales the weights there
     ref_plain = oracle_routing(w, inp)
     assert not np.allclose(got["w"], ref_plain["w"], rtol=1e-3)
+
+
+@pytest.mark.parametrize("T,path,x_dtype", [(1, moe.MOE_PATH_AUTO, "bf16"), (4, moe.MOE_PATH_GEMV, "bf16"),
+                                            (24, moe.MOE_PATH_GEMV, "bf16"), (200, moe.MOE_PATH_AUTO, "bf16"),
+                                            (8, moe.MOE_PATH_GEMM, "bf16"), (3, moe.MOE_PATH_AUTO, "f32"),
+                                            (40, moe.MOE_PATH_GEMM, "f32")])
+def test_sigmoid_gated_shared_expert(T, path, x_dtype):
+    # shared_gate: router row E is a gate vector g and the shared expert's
+    # output is scaled by sigmoid(x_t . g); the fused decode kernel at T = 1,
+    # 3 and 4, the GEMV kernels at T = 24, the grouped GEMMs at T = 200, 8, 40
+    w = custom(f"sgate{T}{x_dtype}", T=T, x_dtype=x_dtype)
+    inp = layer_inputs(w)
+    g = mw.draw_shared_gate(w)
+    d = device_inputs(w, inp)
+    d["router_w"] = torch.cat([d["router_w"], torch.from_numpy(g)[None].to(d["router_w"].device)]).contiguous()
+    layer = make_layer(w, path=path, shared_gate=True)
+    got, y = gpu_run(w, inp, layer, dev_in=d)
+    layer.close()
+    check_routing(got, oracle_routing(w, inp))
+    toks = sample_tokens(w.T, 40)
+    got_y = y_host(y)[toks]
+    check_y(got_y, oracle_y(w, inp, toks, shared_gate_w=g), f"sigmoid-gated shared expert, T={T}")
+    # the gate matters on these inputs: the ungated layer is outside the tolerance
+    plain = oracle_y(w, inp, toks)
+    assert np.linalg.norm(got_y - plain) / np.linalg.norm(plain) > 10 * 1e-2
+
+
+def test_shared_gate_needs_a_shared_expert():
+    with pytest.raises(moe.MoeError):
+        moe.MoeLayer(512, 64, 256, 4, 16, has_shared=False, shared_gate=True)
