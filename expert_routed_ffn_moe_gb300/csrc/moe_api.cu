@@ -41,6 +41,8 @@ struct moe_ctx {
 namespace {
 
 constexpr long long kDefaultSpinNs = 1000000000LL;  // 1 s
+// Largest T the automatic path sends to the small-T kernels (measured crossover, see moe_forward).
+constexpr int kGemvMaxT = 3;
 constexpr int kGemvSmemLimit = 200 * 1024;           // dynamic shared memory of the GEMV kernels
 constexpr int kDecodeReps = 8;                       // copies of the decode kernel's broadcast data
 

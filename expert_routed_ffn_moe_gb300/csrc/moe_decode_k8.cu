@@ -1,0 +1,8 @@
+// The fused decode kernel instantiated for at most 8 tokens (MAXT = 8).
+#include "moe_decode_kernel.cuh"
+
+namespace moe {
+
+const void* decode_kernel_maxt8(const Shapes& s) { return pick_shape<8>(s); }
+
+}  // namespace moe

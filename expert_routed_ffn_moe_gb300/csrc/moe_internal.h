@@ -15,10 +15,6 @@ constexpr int kMaxExperts = 256;
 constexpr int kMaxTopK = 32;
 constexpr int kChunk = 32;       // tokens per grouping chunk (one bit each in a 32-bit mask)
 constexpr int kBM = 128;         // rows (tokens) per grouped-GEMM tile
-// Largest T the automatic path sends to the GEMV kernels.  Measured per layer (d = 2048, 256 experts,
-// inter 512, top-8 + shared; fused kernel vs grouped GEMMs): T = 1: 18 vs 69 us, 2: 40 vs 78, 3: 65 vs 89,
-// 4: 100 vs 87, 8: 261 vs 126 -- the grouped GEMMs win from T = 4.
-constexpr int kGemvMaxT = 3;
 
 // m-tile of the grouped GEMM: rows [row0, row0 + rows) of the expert-grouped
 // buffers belong to expert `e` (e == E is the shared expert).

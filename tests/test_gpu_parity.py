@@ -360,3 +360,11 @@ def test_sigmoid_gated_shared_expert(T, path, x_dtype):
 def test_shared_gate_needs_a_shared_expert():
     with pytest.raises(moe.MoeError):
         moe.MoeLayer(512, 64, 256, 4, 16, has_shared=False, shared_gate=True)
+
+
+@pytest.mark.parametrize("T", [2, 3, 5, 8, 13, 16])
+def test_fused_kernel_each_token_bound(T):
+    # the fused kernel is instantiated for token bounds 1, 2, 4, 8 and 16; run
+    # each bound at the decode shapes (d = 2048, 256 experts, inter 512,
+    # top-8 + shared), at and between the bounds
+    full_case(mw.Workload(f"fused_T{T}", T=T, cid=91), path=moe.MOE_PATH_GEMV)
