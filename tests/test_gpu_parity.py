@@ -362,9 +362,26 @@ def test_shared_gate_needs_a_shared_expert():
         moe.MoeLayer(512, 64, 256, 4, 16, has_shared=False, shared_gate=True)
 
 
-@pytest.mark.parametrize("T", [2, 3, 5, 8, 13, 16])
+@pytest.mark.parametrize("T", [2, 3, 5, 8, 10])
 def test_fused_kernel_each_token_bound(T):
     # the fused kernel is instantiated for token bounds 1, 2, 4, 8 and 16; run
     # each bound at the decode shapes (d = 2048, 256 experts, inter 512,
-    # top-8 + shared), at and between the bounds
+    # top-8 + shared), at and between the bounds (T = 10 is the largest whose
+    # activations fit in shared memory at these shapes)
     full_case(mw.Workload(f"fused_T{T}", T=T, cid=91), path=moe.MOE_PATH_GEMV)
+
+
+def test_fused_kernel_sixteen_tokens():
+    full_case(custom("fused_T16", T=16), path=moe.MOE_PATH_GEMV)
+
+
+def test_fused_kernel_rejects_tokens_beyond_shared_memory():
+    # T = 11 at the decode shapes: neither the fused kernel nor the GEMV
+    # kernels hold its activations; the forced small-T path says so
+    w = mw.Workload("fused_T11", T=11, cid=91)
+    layer = make_layer(w, path=moe.MOE_PATH_GEMV)
+    d = device_inputs(w, layer_inputs(w))
+    with pytest.raises(moe.MoeError) as e:
+        layer.forward(d["x"], d["router_w"], d["router_b"], d["gate_up"], d["down"], d["shared"])
+    assert e.value.code == moe.MOE_ERR_UNSUPPORTED
+    layer.close()
