@@ -376,9 +376,10 @@ def test_fused_kernel_sixteen_tokens():
 
 
 def test_fused_kernel_rejects_tokens_beyond_shared_memory():
-    # T = 11 at the decode shapes: neither the fused kernel nor the GEMV
-    # kernels hold its activations; the forced small-T path says so
-    w = mw.Workload("fused_T11", T=11, cid=91)
+    # T = 12 at the decode shapes: neither the fused kernel (up to T = 10
+    # here) nor the GEMV kernels (up to T = 11) hold its activations in
+    # shared memory; the forced small-T path says so
+    w = mw.Workload("fused_T12", T=12, cid=91)
     layer = make_layer(w, path=moe.MOE_PATH_GEMV)
     d = device_inputs(w, layer_inputs(w))
     with pytest.raises(moe.MoeError) as e:
