@@ -79,16 +79,18 @@ def kernel_source_hash(kernel):
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(kernel):
-    """DRAM bytes per launch (read + write) of `kernel` from the ncu summaries under
-    profiles/, if one was taken of the current source; else None."""
+def profiled_traffic(kernel, workload):
+    """DRAM bytes per launch (read + write) of `kernel` on `workload` from the ncu
+    summaries under profiles/, if one was taken of the current source on that
+    workload; else None."""
     want = kernel_source_hash(kernel)
     for path in sorted(glob.glob(os.path.join(HERE, "profiles", "*.md"))):
         with open(path) as fh:
             for line in fh:
-                m = re.match(r"traffic-record: kernel=(\S+) source_sha256=(\w+) bytes_per_launch=(\d+)", line.strip())
-                if m and m.group(1) == kernel and m.group(2) == want:
-                    return int(m.group(3))
+                m = re.match(r"traffic-record: kernel=(\S+) workload=(\S+) source_sha256=(\w+) bytes_per_launch=(\d+)",
+                             line.strip())
+                if m and m.group(1) == kernel and m.group(2) == workload and m.group(3) == want:
+                    return int(m.group(4))
     return None
 GRAPH_STEPS = 50  # steps per captured graph; longer runs replay it
 EVENT_EVERY = 5   # steps between two event-timed launches of the dominant kernel
@@ -327,6 +329,9 @@ def run_ours(args, rank, world, dev):
     dom = dominant_kernel(eff_path)
 
     whole_layer = eff_path == moe.MOE_PATH_GEMV  # the dominant kernel is the whole layer
+    # the configuration a traffic record must have been taken on (per-launch traffic
+    # does not depend on the number of stacked layers)
+    traffic_key = w.name + ("+shared_gate" if args.shared_gate else "") + (f"+chunk{args.chunk}" if args.chunk else "")
     if layers > 1:
         # stacked layers with fixed weights: a layer's blocks may start on its
         # weights while the previous layer's kernel finishes (moe_set_overlap)
@@ -442,7 +447,7 @@ def run_ours(args, rank, world, dev):
         per_launch = statistics.mean(c["layer_bytes"] for c in costs)
         achieved = per_launch / (kern_avg_ms / 1e3) / 1e9
         roof = dict(bound="hbm", achieved=round(achieved, 1), peak=peaks["hbm_gbs"], unit="GB/s",
-                    frac=round(achieved / peaks["hbm_gbs"], 4), traffic=profiled_traffic("decode_fused_kernel"),
+                    frac=round(achieved / peaks["hbm_gbs"], 4), traffic=profiled_traffic("decode_fused_kernel", traffic_key),
                     kernel="decode_fused_kernel (whole layer)", algorithmic_bytes_per_launch=int(per_launch),
                     avg_launch_us=round(kern_avg_ms * 1e3, 2), peak_source=peaks["source"])
     else:
@@ -457,7 +462,7 @@ def run_ours(args, rank, world, dev):
         else:
             roof = dict(bound="tensor", achieved=round(tfs, 1), peak=peaks["bf16_tflops"], unit="TFLOP/s",
                         frac=round(tc_frac, 4), traffic=None)
-        roof["traffic"] = profiled_traffic("grouped_gemm_kernel<gate_up>")
+        roof["traffic"] = profiled_traffic("grouped_gemm_kernel<gate_up>", traffic_key)
         roof.update(kernel="grouped_gemm_kernel<gate_up>", algorithmic_bytes_per_launch=int(per_launch_b),
                     algorithmic_flops_per_launch=int(per_launch_f), avg_launch_us=round(kern_avg_ms * 1e3, 2),
                     tensor_frac=round(tc_frac, 4), hbm_frac=round(hbm_frac, 4), peak_source=peaks["source"])

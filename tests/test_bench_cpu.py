@@ -19,14 +19,16 @@ def test_traffic_record_matches_only_current_source(tmp_path, monkeypatch):
     monkeypatch.setattr(bench, "CSRC", str(root / "expert_routed_ffn_moe_gb300" / "csrc"))
     h = bench.kernel_source_hash("decode_fused_kernel")
     (root / "profiles" / "k.md").write_text(
-        f"text\ntraffic-record: kernel=decode_fused_kernel source_sha256={h} bytes_per_launch=12345\n")
-    assert bench.profiled_traffic("decode_fused_kernel") == 12345
-    assert bench.profiled_traffic("grouped_gemm_kernel<gate_up>") is None
-    src = root / "expert_routed_ffn_moe_gb300" / "csrc" / "moe_decode.cu"
+        f"text\ntraffic-record: kernel=decode_fused_kernel workload=decode source_sha256={h} bytes_per_launch=12345\n")
+    assert bench.profiled_traffic("decode_fused_kernel", "decode") == 12345
+    # another workload (another token count, a variant) moves other bytes
+    assert bench.profiled_traffic("decode_fused_kernel", "sweep_T2") is None
+    assert bench.profiled_traffic("grouped_gemm_kernel<gate_up>", "decode") is None
+    src = root / "expert_routed_ffn_moe_gb300" / "csrc" / "moe_decode_kernel.cuh"
     src.write_text(src.read_text() + "\n// a comment changes no kernel\n")
-    assert bench.profiled_traffic("decode_fused_kernel") == 12345
+    assert bench.profiled_traffic("decode_fused_kernel", "decode") == 12345
     src.write_text(src.read_text() + "\nstatic int changed_code = 1;\n")
-    assert bench.profiled_traffic("decode_fused_kernel") is None
+    assert bench.profiled_traffic("decode_fused_kernel", "decode") is None
 
 
 def test_aggregate_single_rank():
