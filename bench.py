@@ -325,7 +325,7 @@ def run_ours(args, rank, world, dev):
     path = moe.MOE_PATH_AUTO if args.path == "auto" else (moe.MOE_PATH_GEMV if args.path == "gemv"
                                                           else moe.MOE_PATH_GEMM)
     moe.moe_set_path(ctx.ctx, path)
-    eff_path = path if path != moe.MOE_PATH_AUTO else (moe.MOE_PATH_GEMV if w.T <= 5 else moe.MOE_PATH_GEMM)  # the library's rule
+    eff_path = path if path != moe.MOE_PATH_AUTO else (moe.MOE_PATH_GEMV if w.T <= 7 else moe.MOE_PATH_GEMM)  # the library's rule
     dom = dominant_kernel(eff_path)
 
     whole_layer = eff_path == moe.MOE_PATH_GEMV  # the dominant kernel is the whole layer

@@ -43,8 +43,9 @@ namespace {
 constexpr long long kDefaultSpinNs = 1000000000LL;  // 1 s
 // Largest T the automatic path sends to the small-T kernels.  Measured per layer (d = 2048, 256
 // experts, inter 512, top-8 + shared; fused kernel vs grouped GEMMs): T = 1: 19 vs 71 us, 2: 31 vs 82,
-// 3: 47 vs 88, 4: 66 vs 86, 5: 95 vs 117, 6: 124 vs 121, 8: 146 vs 126 -- the GEMMs win from T = 6.
-constexpr int kGemvMaxT = 5;
+// 3: 45 vs 88, 4: 61 vs 86, 5: 80 vs 117, 6: 102 vs 121, 7: 122 vs 123, 8: 130 vs 126 -- the GEMMs
+// win from T = 8.
+constexpr int kGemvMaxT = 7;
 constexpr int kGemvSmemLimit = 200 * 1024;           // dynamic shared memory of the GEMV kernels
 constexpr int kDecodeReps = 8;                       // copies of the decode kernel's broadcast data
 

@@ -255,6 +255,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const DecodeA
   __shared__ int act_row[kMaxExperts + 1];      // first grouped h row of each active expert
   __shared__ float act_w[kMaxExperts + 1][MAXT];
   __shared__ float sgate_s[MAXT];               // the shared expert's weight per token
+  // grouped h row p -> (active expert, token): phase C walks a chunk's rows (MAXT > 1)
+  __shared__ uint16_t pair_a[MAXT > 1 ? MAXT * (kMaxTopK + 1) : 1];
+  __shared__ uint8_t pair_t[MAXT > 1 ? MAXT * (kMaxTopK + 1) : 1];
   __shared__ int n_act_s, flag_s;
   __shared__ unsigned ep_s;  // this launch's epoch: the tag of every value it publishes
   __shared__ int warp_tot[kWarps];
@@ -515,6 +518,12 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const DecodeA
         act_e[pos] = tid;
         act_m[pos] = m;
         act_row[pos] = excl & 0xffff;
+        for (int t = 0, i = 0; t < MAXT; ++t)
+          if ((m >> t) & 1u) {
+            pair_a[(excl & 0xffff) + i] = (uint16_t)pos;
+            pair_t[(excl & 0xffff) + i] = (uint8_t)t;
+            ++i;
+          }
         for (int t = 0; t < MAXT; ++t) {
           float wt = 0.f;
           if (t < s.T)
@@ -532,6 +541,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const DecodeA
           act_m[n_routed] = (s.T >= 32) ? 0xffffffffu : ((1u << s.T) - 1u);
           act_row[n_routed] = tk;
           for (int t = 0; t < MAXT; ++t) act_w[n_routed][t] = t < s.T ? sgate_s[t] : 0.f;
+          for (int t = 0; t < s.T; ++t) {
+            pair_a[tk + t] = (uint16_t)n_routed;
+            pair_t[tk + t] = (uint8_t)t;
+          }
         }
         n_act_s = n_routed + (s.has_shared ? 1 : 0);
       }
@@ -702,22 +715,46 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const DecodeA
           }
           part[0] += (ps[0] + ps[1]) + ps[2];
         }
-        for (int qa = 0; qa < na && MAXT > 1; ++qa) {
-          const int a = a0 + qa;
-          uint2 wv[2 * NCI];
+        if (MAXT > 1) {
+          // the chunk's (expert, token) pairs are the contiguous grouped h rows
+          // p0 .. p1 - 1 (experts ascending, tokens ascending within one);
+          // three pairs per step with independent dot products, so that their
+          // shared-memory loads and FMA chains overlap (one expert at a time,
+          // token by token, the loop was a chain of dependent latencies)
+          const int p0 = act_row[a0];
+          const int p1 = (a0 + na < n_act) ? act_row[a0 + na] : (int)pairs;
+          for (int p = p0; p < p1; p += 3) {
+            float dd[3], ww[3];
+            int tt[3];
 #pragma unroll
-          for (int cc = 0; cc < 2 * NCI; ++cc) wv[cc] = base[(size_t)qa * (s.I / 4) + 32 * cc];
-          const unsigned mm = act_m[a];
-          const int row0 = act_row[a];
+            for (int u = 0; u < 3; ++u) {
+              dd[u] = 0.f;
+              ww[u] = 0.f;
+              tt[u] = -1;
+              const int pu = p + u;
+              if (pu < p1) {
+                const int a = pair_a[pu];
+                tt[u] = pair_t[pu];
+                ww[u] = act_w[a][tt[u]];
+                const uint2* wr = base + (size_t)(a - a0) * (s.I / 4);
+                const float4* hr = reinterpret_cast<const float4*>(big + (size_t)pu * s.I) + lane;
+                float d0 = 0.f, d1 = 0.f;
 #pragma unroll
-          for (int t = 0; t < MAXT; ++t) {
-            if ((mm >> t) & 1u) {
-              const int row = row0 + __popc(mm & ((1u << t) - 1u));
-              const float4* hr = reinterpret_cast<const float4*>(big + (size_t)row * s.I) + lane;
-              float dsum = 0.f;
+                for (int cc = 0; cc < 2 * NCI; cc += 2) {
+                  d0 = dot4(wr[32 * cc], hr[32 * cc], d0);
+                  d1 = dot4(wr[32 * (cc + 1)], hr[32 * (cc + 1)], d1);
+                }
+                dd[u] = d0 + d1;
+              }
+            }
+            // every token's sum takes a term (zero unless the pair is its own):
+            // a conditional update indexed by the pair's token would move
+            // part[] to local memory
 #pragma unroll
-              for (int cc = 0; cc < 2 * NCI; ++cc) dsum = dot4(wv[cc], hr[32 * cc], dsum);
-              part[t] = fmaf(act_w[a][t], dsum, part[t]);
+            for (int u = 0; u < 3; ++u) {
+              const float v = ww[u] * dd[u];
+#pragma unroll
+              for (int t = 0; t < MAXT; ++t) part[t] += (tt[u] == t) ? v : 0.f;
             }
           }
         }
