@@ -43,6 +43,9 @@ def _cfg(**kw):
     (dict(inter=100, shared_inter=100), moe.MOE_ERR_UNSUPPORTED),
     (dict(n_experts=300), moe.MOE_ERR_UNSUPPORTED),
     (dict(shared_inter=256), moe.MOE_ERR_UNSUPPORTED),
+    (dict(bias_select_only=2), moe.MOE_ERR_ARG),
+    (dict(shared_gate=2), moe.MOE_ERR_ARG),
+    (dict(shared_gate=1, has_shared=0), moe.MOE_ERR_ARG),
 ])
 def test_init_rejects_bad_configs_before_any_device_call(lib, kw, code):
     h = ctypes.c_void_p()
@@ -59,3 +62,16 @@ def test_null_arguments(lib):
     assert lib.moe_set_path(None, 0) == moe.MOE_ERR_ARG
     assert lib.moe_status(None) == moe.MOE_ERR_ARG
     lib.moe_destroy(None)
+
+
+def test_binding_config_matches_header():
+    # the ctypes mirror of moe_config lists the header's int fields in order
+    import os
+    import re
+
+    hdr = open(os.path.join(os.path.dirname(moe.__file__), "..", "include", "moe.h")).read()
+    body = re.search(r"typedef struct moe_config \{(.*?)\} moe_config;", hdr, re.S).group(1)
+    body = re.sub(r"/\*.*?\*/", "", body, flags=re.S)
+    fields = re.findall(r"\bint\s+(\w+)\s*;", body)
+    assert [n for n, _ in moe.moe_config._fields_] == fields
+    assert all(t is ctypes.c_int for _, t in moe.moe_config._fields_)
