@@ -7,6 +7,7 @@ with it.  See ``moe_oracle.py`` for the steps and the passages they follow.
 from .moe_oracle import (  # noqa: F401
     as_f64,
     decode_bf16,
+    dequant_affine4,
     group,
     moe_layer,
     route,
@@ -16,4 +17,5 @@ from .moe_oracle import (  # noqa: F401
     silu,
     softmax,
     swiglu_ffn,
+    unpack_u4,
 )

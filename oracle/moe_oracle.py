@@ -35,6 +35,14 @@ Variants the pages do not describe (plain readings, each pinned on its own):
   and the picks' weights are the softmax of the unbiased logits over them.
 - sigmoid-gated shared expert: o_shared(x_t) is scaled by sigmoid(x_t . g) for
   a gate vector g of d fp32 values (no bias).
+- 4-bit group-affine expert weights ("Optimizing on-device inference for Apple
+  Silicon", section "Dequantizing weights during matrix multiplication": the
+  checkpoint stores the experts in 4 bits and the kernels expand them inside
+  the multiplication).  Reading: along each weight row, groups of 64
+  consecutive input columns share one scale and one bias (bf16); a weight is
+  scale * q + bias for its 4-bit code q in 0..15; eight codes are packed per
+  32-bit word, the lowest nibble first.  The layer is then the same layer over
+  the expanded weights (``dequant_affine4`` and ``moe_layer(weights_f64=True)``).
 
 Library primitives used as steps: numpy matmul (a dot product per output
 element), ``numpy.exp``, ``numpy.argsort`` (stable) and ``numpy.bincount``.
@@ -138,6 +146,24 @@ def swiglu_ffn(x_rows: np.ndarray, gate_up: np.ndarray, down: np.ndarray) -> np.
     return h @ down.T
 
 
+def unpack_u4(words: np.ndarray) -> np.ndarray:
+    """uint32 words [..., n] -> 4-bit codes [..., 8 n] (uint8), lowest nibble first."""
+    w = np.ascontiguousarray(words, dtype=np.uint32)
+    shifts = np.arange(8, dtype=np.uint32) * 4
+    codes = (w[..., None] >> shifts) & np.uint32(15)
+    return codes.reshape(*w.shape[:-1], w.shape[-1] * 8).astype(np.uint8)
+
+
+def dequant_affine4(words: np.ndarray, scales: np.ndarray, biases: np.ndarray, group: int = 64) -> np.ndarray:
+    """Expanded weights, fp64 [..., K]: scale[g] * q + bias[g] for the group g = k // group of
+    each column k.  words uint32 [..., K / 8]; scales, biases bf16 bits [..., K / group]."""
+    q = unpack_u4(words).astype(np.float64)
+    s = np.repeat(decode_bf16(scales), group, axis=-1)
+    b = np.repeat(decode_bf16(biases), group, axis=-1)
+    assert q.shape == s.shape == b.shape, (q.shape, s.shape, b.shape)
+    return s * q + b
+
+
 def sigmoid(z: np.ndarray) -> np.ndarray:
     """sigmoid(z) = 1 / (1 + exp(-z))."""
     with np.errstate(over="ignore"):
@@ -146,7 +172,7 @@ def sigmoid(z: np.ndarray) -> np.ndarray:
 
 def moe_layer(x, router_w, router_b, gate_up, down, shared, k, *, x_bf16: bool,
               shared_inter: int | None = None, tokens=None, expert_ids=None, bias_select_only: bool = False,
-              shared_gate_w=None):
+              shared_gate_w=None, weights_f64: bool = False):
     """Steps 1-8 for the token rows ``tokens`` (default: all).
 
     x        [T, d]  fp32 values, or bf16 bits when ``x_bf16``
@@ -159,6 +185,10 @@ def moe_layer(x, router_w, router_b, gate_up, down, shared, k, *, x_bf16: bool,
              the softmax of the unbiased logits over the picks.
     shared_gate_w  [d] fp32 gate vector, or None: the shared expert's output
              is scaled by sigmoid(x_t . shared_gate_w).
+    weights_f64  the expert weights are given as float64 values (for example
+             expanded 4-bit weights) instead of bf16 bits: gate_up [n, 2I, d],
+             down [n, d, I], and shared, if any, as the pair (gate_up [2I_s, d],
+             down [d, I_s]).
 
     Returns dict(y [n_tok, d] fp64, idx, w, margin, logits) for those tokens."""
     xs = as_f64(x, x_bf16)
@@ -178,13 +208,19 @@ def moe_layer(x, router_w, router_b, gate_up, down, shared, k, *, x_bf16: bool,
         if rows.size == 0:
             continue
         j = where[e]
-        o = swiglu_ffn(xs[rows], decode_bf16(gate_up[j]), decode_bf16(down[j]))
+        if weights_f64:
+            o = swiglu_ffn(xs[rows], np.asarray(gate_up[j], dtype=np.float64), np.asarray(down[j], dtype=np.float64))
+        else:
+            o = swiglu_ffn(xs[rows], decode_bf16(gate_up[j]), decode_bf16(down[j]))
         w_e = w[rows, np.argmax(idx[rows] == e, axis=1)]
         y[rows] += w_e[:, None] * o
     if shared is not None:
-        i_s = shared_inter if shared_inter is not None else len(shared) // (3 * d)
-        sh = decode_bf16(shared)
-        o_s = swiglu_ffn(xs, sh[: 2 * i_s * d].reshape(2 * i_s, d), sh[2 * i_s * d:].reshape(d, i_s))
+        if weights_f64:
+            o_s = swiglu_ffn(xs, np.asarray(shared[0], dtype=np.float64), np.asarray(shared[1], dtype=np.float64))
+        else:
+            i_s = shared_inter if shared_inter is not None else len(shared) // (3 * d)
+            sh = decode_bf16(shared)
+            o_s = swiglu_ffn(xs, sh[: 2 * i_s * d].reshape(2 * i_s, d), sh[2 * i_s * d:].reshape(d, i_s))
         if shared_gate_w is not None:
             o_s = sigmoid(xs @ np.asarray(shared_gate_w, dtype=np.float64))[:, None] * o_s
         y += o_s

@@ -411,6 +411,77 @@ def test_shared_gate_scales_only_the_shared_expert():
         assert np.allclose(gated2[t], routed[t] + s_t * shared_part[t], atol=1e-12, rtol=0)
 
 
+# ------------------------------------------------------- 4-bit group-affine weights
+
+def _bf16_value(bits: int) -> float:
+    # an independent bf16 decoder: the bits are the high half of an fp32
+    import struct
+    return struct.unpack(">f", ((bits & 0xFFFF) << 16).to_bytes(4, "big"))[0]
+
+
+def test_unpack_u4_hand_worked():
+    words = np.array([0x76543210, 0xFEDCBA98], dtype=np.uint32)
+    assert list(oracle.unpack_u4(words)) == list(range(16))
+    assert list(oracle.unpack_u4(np.array([0xF0F0F0F0], dtype=np.uint32))) == [0, 15] * 4
+
+
+def test_dequant_affine4_hand_worked():
+    # one row of 128 columns, two groups: scale 0.5 / bias -1 with every code
+    # 3 (-> 0.5), then scale 2 / bias 0.25 with codes 0, 15, 0, 15, ...
+    # (-> 0.25, 30.25, ...)
+    words = np.array([[0x33333333] * 8 + [0xF0F0F0F0] * 8], dtype=np.uint32)
+    scales = np.array([[0x3F00, 0x4000]], dtype=np.uint16)
+    biases = np.array([[0xBF80, 0x3E80]], dtype=np.uint16)
+    w = oracle.dequant_affine4(words, scales, biases)
+    assert w.shape == (1, 128)
+    assert np.all(w[0, :64] == 0.5)
+    assert list(w[0, 64:68]) == [0.25, 30.25, 0.25, 30.25]
+    # all-zero codes give the bias, all-15 codes 15 scale + bias
+    z = oracle.dequant_affine4(np.zeros((1, 16), np.uint32), scales, biases)
+    assert np.all(z[0, :64] == -1.0) and np.all(z[0, 64:] == 0.25)
+    f = oracle.dequant_affine4(np.full((1, 16), 0xFFFFFFFF, np.uint32), scales, biases)
+    assert np.all(f[0, :64] == 6.5) and np.all(f[0, 64:] == 30.25)
+
+
+def test_dequant_affine4_brute_force():
+    rng = np.random.default_rng(21)
+    rows, K, g = 3, 256, 64
+    words = rng.integers(0, 2 ** 32, size=(rows, K // 8), dtype=np.uint64).astype(np.uint32)
+    scales = bf16_bits(rng.normal(size=(rows, K // g)) * 0.01)
+    biases = bf16_bits(rng.normal(size=(rows, K // g)) * 0.05)
+    got = oracle.dequant_affine4(words, scales, biases, group=g)
+    for r in range(rows):
+        for k in range(K):
+            q = (int(words[r, k // 8]) >> (4 * (k % 8))) & 15
+            want = _bf16_value(int(scales[r, k // g])) * q + _bf16_value(int(biases[r, k // g]))
+            assert got[r, k] == want, (r, k)
+
+
+def test_layer_on_expanded_4bit_weights():
+    # 4-bit weights whose expansion (q - 8) / 32 is exact in bf16: the layer
+    # on the expanded fp64 weights equals the layer on those bf16 weights
+    rng = np.random.default_rng(22)
+    E, d, inter, k, T = 4, 64, 64, 2, 5
+    x = rng.normal(size=(T, d)).astype(np.float32)
+    wr = (rng.normal(size=(E, d)) * 0.5).astype(np.float32)
+
+    def q4(rows, cols):
+        words = rng.integers(0, 2 ** 32, size=(rows, cols // 8), dtype=np.uint64).astype(np.uint32)
+        sc = np.full((rows, cols // 64), 0x3D00, np.uint16)  # 2^-5
+        bi = np.full((rows, cols // 64), 0xBE80, np.uint16)  # -2^-2
+        return oracle.dequant_affine4(words, sc, bi)
+
+    gu = np.stack([q4(2 * inter, d) for _ in range(E)])
+    dn = np.stack([q4(d, inter) for _ in range(E)])
+    sh = (q4(2 * inter, d), q4(d, inter))
+    assert np.all(gu * 32 == np.round(gu * 32)) and np.abs(gu).max() <= 0.25
+    r64 = oracle.moe_layer(x, wr, None, gu, dn, sh, k, x_bf16=False, weights_f64=True)
+    flat_sh = np.concatenate([bf16_bits(sh[0]).ravel(), bf16_bits(sh[1]).ravel()])
+    rb = oracle.moe_layer(x, wr, None, bf16_bits(gu), bf16_bits(dn), flat_sh, k, x_bf16=False)
+    assert np.array_equal(r64["idx"], rb["idx"])
+    assert np.array_equal(r64["y"], rb["y"])
+
+
 def test_layer_token_permutation_equivariance_and_subsets():
     rng = np.random.default_rng(11)
     x, wr, gu, dn, sh = tiny_layer(rng, T=11, E=7, d=8, inter=4, k=3)
