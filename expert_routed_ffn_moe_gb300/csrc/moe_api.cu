@@ -391,7 +391,8 @@ int moe_route(moe_ctx* ctx, const void* x, int T, const float* router_w, const f
       (offsets && !aligned16(offsets)) || (perm && !aligned16(perm)))
     return MOE_ERR_ALIGN;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  const Shapes s = shapes(ctx, T, top_k);
+  Shapes s = shapes(ctx, T, top_k);
+  s.shared_gate = 0;  // routing only: router_w may hold just the E expert rows
   const bool tensor = use_tensor_router(ctx, s);
   GemmMaps maps;
   memset(&maps, 0, sizeof(maps));

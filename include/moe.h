@@ -104,7 +104,8 @@ typedef struct moe_ctx moe_ctx;
 int moe_init(const moe_config* cfg, moe_ctx** out);
 
 /* Steps 1-4 only, for inspection.  Inputs: x [T, d] (cfg->x_dtype), router_w
- * [E, d] fp32, router_b [E] fp32 (NULL unless cfg->has_router_bias).  Outputs
+ * [E, d] fp32 (a shared-gate row E, if present, is not read), router_b [E]
+ * fp32 (NULL unless cfg->has_router_bias).  Outputs
  * (caller-owned device buffers): idx [T, top_k] int32 (ascending expert id per
  * row), w [T, top_k] fp32, counts [E] int32, offsets [E + 1] int32 (exclusive
  * prefix of counts; offsets[E] = T * top_k), perm [T * top_k] int32 (token ids
