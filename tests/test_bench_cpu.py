@@ -36,3 +36,28 @@ def test_aggregate_single_rank():
     assert ms_step == pytest.approx(10.0)
     assert value == pytest.approx(5 / 0.010)
     assert e2e == pytest.approx(5 / 0.020)
+
+
+def test_algorithmic_bytes_and_flops_per_unit():
+    import numpy as np
+
+    import moe_workloads as mw
+
+    expert = 3 * 2048 * 512 * 2  # gate_up [1024, 2048] + down [2048, 512], bf16
+    assert expert == 6_291_456
+    # decode: one token, 8 distinct routed experts + the shared one, the fp32
+    # router, x and y in bf16
+    c = bench.layer_costs(mw.WORKLOADS["decode"], np.arange(8)[None, :] * 3)
+    assert c["distinct"] == 9
+    assert c["layer_bytes"] == 9 * expert + 256 * 2048 * 4 + 2 * 2048 * 2 == 58_728_448
+    assert c["layer_flops"] == 2 * 9 * 3 * 2048 * 512
+    # balanced prefill: all 256 experts + shared; gate/up reads two thirds of
+    # each expert plus the token rows once
+    w = mw.WORKLOADS["prefill_balanced"]
+    idx = (np.arange(w.T * 8).reshape(w.T, 8)) % 256
+    c = bench.layer_costs(w, idx)
+    assert c["gate_up_bytes"] == 257 * 2 * 512 * 2048 * 2 + 4096 * 2048 * 2 == 1_094_713_344
+    assert c["gate_up_flops"] == 2 * 4096 * 9 * 2048 * 1024
+    # the shared-gate variant adds its fp32 gate row to the router bytes
+    c2 = bench.layer_costs(w, idx, shared_gate=True)
+    assert c2["layer_bytes"] - c["layer_bytes"] == 2048 * 4
