@@ -24,6 +24,11 @@ each tensor from its own ``SeedSequence``):
 * shared gate      (the sigmoid-gated shared-expert variant) g ~ N(0, 0.9^2 / d),
   fp32 [d]: with x ~ N(0, 1) the gate logit x . g has a spread of about 0.9,
   so the gates cover most of (0, 1).
+* 4-bit experts    (the 4-bit group-affine variant) per weight matrix: uniformly
+  random 32-bit words (eight uniform 4-bit codes each), and per 64-column group
+  a bf16 scale s = 0.02 / sqrt(21.25) * (1 + 0.1 N(0, 1)) and bias -7.5 s (21.25
+  is the variance of a uniform code in 0..15), so that the expanded weights have
+  mean ~0 and spread ~0.02 like the bf16 experts.
 
 Each expert is drawn from its own stream, so a caller that needs only a few
 experts (the oracle on a sample of tokens) can draw just those.
@@ -46,7 +51,7 @@ import numpy as np
 SEED_BASE = 20261202
 
 # tensor-kind tags for SeedSequence keys
-_X, _X_REDRAW, _ROUTER_W, _GATE_UP, _DOWN, _SHARED, _SHARED_GATE = range(7)
+_X, _X_REDRAW, _ROUTER_W, _GATE_UP, _DOWN, _SHARED, _SHARED_GATE, _Q4 = range(8)
 
 
 @dataclasses.dataclass(frozen=True)
@@ -132,6 +137,22 @@ def draw_expert(w: Workload, layer: int, e: int):
     gu = _normal(0.02, 2 * w.I * w.d, w.seed, layer, _GATE_UP, e)
     dn = _normal(0.02, w.d * w.I, w.seed, layer, _DOWN, e)
     return (f32_to_bf16_bits(gu).reshape(2 * w.I, w.d), f32_to_bf16_bits(dn).reshape(w.d, w.I))
+
+
+def _q4_matrix(rows: int, cols: int, *key: int):
+    rng = _rng(*key)
+    words = rng.integers(0, 2 ** 32, size=(rows, cols // 8), dtype=np.uint64).astype(np.uint32)
+    s = np.float32(0.02 / math.sqrt(21.25)) * (1 + np.float32(0.1) * rng.standard_normal((rows, cols // 64),
+                                                                                          dtype=np.float32))
+    return words, f32_to_bf16_bits(s), f32_to_bf16_bits(np.float32(-7.5) * s)
+
+
+def draw_expert_q4(w: Workload, layer: int, e: int):
+    """One routed expert in 4 bits (``e = -1``: the shared expert): for gate_up [2I, d]
+    and down [d, I], (words uint32 [rows, cols / 8], scales, biases bf16 [rows, cols / 64])."""
+    inter = w.I if e >= 0 else w.I_s
+    return (_q4_matrix(2 * inter, w.d, w.seed, layer, _Q4, e + 1, 0),
+            _q4_matrix(w.d, inter, w.seed, layer, _Q4, e + 1, 1))
 
 
 def draw_experts(w: Workload, layer: int = 0, experts=None, threads: int = 16):

@@ -525,3 +525,18 @@ def test_skewed_bias_matches_recipe():
     w = mw.WORKLOADS["prefill_skewed"]
     _, b = mw.draw_router(w)
     assert b[0] == 0.0 and abs(b[1] - 1.2 * math.log(0.5)) < 1e-6 and np.all(np.diff(b) < 0)
+
+
+def test_4bit_inputs_recipe():
+    # the seeded 4-bit experts expand to weights of mean ~0 and spread ~0.02,
+    # like the bf16 experts; codes are uniform over 0..15
+    w = mw.WORKLOADS["decode"]
+    (gu, dn) = mw.draw_expert_q4(w, 0, 5)
+    assert gu[0].shape == (2 * w.I, w.d // 8) and gu[1].shape == (2 * w.I, w.d // 64)
+    assert dn[0].shape == (w.d, w.I // 8) and dn[2].shape == (w.d, w.I // 64)
+    W = oracle.dequant_affine4(*gu)
+    assert abs(W.mean()) < 1e-3 and 0.019 < W.std() < 0.021
+    counts = np.bincount(oracle.unpack_u4(gu[0]).ravel(), minlength=16)
+    assert counts.min() > 0.95 * counts.mean() and counts.max() < 1.05 * counts.mean()
+    sh = mw.draw_expert_q4(w, 0, -1)
+    assert not np.array_equal(sh[0][0], mw.draw_expert_q4(w, 0, 0)[0][0])
