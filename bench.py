@@ -12,6 +12,13 @@ Workloads (``--workload``, default ``decode``):
   prefill_skewed    same with the Zipf-like router bias.
   sweep_T<n>        one layer at T = n.
 
+The default run (decode) prints the decode figures as the line's ``value`` and
+adds the metric's other half as two nested objects, ``prefill_balanced`` and
+``prefill_skewed``, each measured the same way (its own value, roofline with
+both the HBM and the tensor fraction, e2e, cpu_baseline and clocks);
+``--no-prefill`` leaves them out.  Every roofline gives its fraction of the
+measured peak (``frac``) and of the nominal one (``frac_of_nominal``).
+
 Timing: W untimed warm-up steps, then exactly K steps replayed from CUDA graphs
 and bracketed by a barrier and a device synchronisation on both sides, CUDA
 events on the launching stream, max over ranks.  The dominant kernel of the
@@ -94,6 +101,29 @@ def profiled_traffic(kernel, workload):
     return None
 GRAPH_STEPS = 50  # steps per captured graph; longer runs replay it
 EVENT_EVERY = 5   # steps between two event-timed launches of the dominant kernel
+
+
+# Nominal GB300 figures, reported beside the measured ones: HBM3e ~8 TB/s and
+# 2.25 PFLOP/s dense bf16 on the tensor cores.
+NOMINAL = dict(hbm_gbs=8000.0, bf16_tflops=2250.0)
+
+
+def with_nominal(roof):
+    """Add the fractions of the nominal peaks to a roofline object (its own
+    ``frac`` stays against the measured peak)."""
+    if roof.get("unit") == "GB/s":
+        roof["frac_of_nominal"] = round(roof["achieved"] / NOMINAL["hbm_gbs"], 4)
+        roof["nominal_peak"] = NOMINAL["hbm_gbs"]
+    else:
+        roof["frac_of_nominal"] = round(roof["achieved"] / NOMINAL["bf16_tflops"], 4)
+        roof["nominal_peak"] = NOMINAL["bf16_tflops"]
+    if "hbm_frac" in roof:
+        roof["hbm_frac_of_nominal"] = round(roof["hbm_frac"] * roof.get("_hbm_peak", 0) / NOMINAL["hbm_gbs"], 4)
+        roof["tensor_frac_of_nominal"] = round(roof["tensor_frac"] * roof.get("_tc_peak", 0) / NOMINAL["bf16_tflops"],
+                                               4)
+        roof.pop("_hbm_peak", None)
+        roof.pop("_tc_peak", None)
+    return roof
 
 
 def load_peaks():
@@ -297,14 +327,19 @@ def replica_layer(layer: int, rank: int) -> int:
 
 
 # ------------------------------------------------------------------ main arm
-def run_ours(args, rank, world, dev):
+def run_ours(args, rank, world, dev, workload=None, cpu_seconds=None, chunk=None):
+    """One workload (default: ``args.workload``) timed through the library;
+    returns its JSON object on rank 0 (None elsewhere)."""
     import torch
 
     import expert_routed_ffn_moe_gb300 as moe
 
     moe.build()
-    w = mw.WORKLOADS[args.workload]
-    layers = args.layers or w.layers
+    main_run = workload is None
+    w = mw.WORKLOADS[workload or args.workload]
+    layers = (args.layers if main_run else 0) or w.layers
+    chunk = args.chunk if chunk is None else chunk
+    cpu_seconds = args.cpu_seconds if cpu_seconds is None else cpu_seconds
     peaks = load_peaks()
     torch.cuda.set_device(dev)
     stream = torch.cuda.Stream(device=dev)
@@ -317,11 +352,11 @@ def run_ours(args, rank, world, dev):
     yd_all = torch.empty_like(xd_all)
     yh_all = torch.empty_like(xh_all).pin_memory()
     xh, xd, yd, yh = list(xh_all), list(xd_all), list(yd_all), list(yh_all)
-    max_tokens = args.chunk if args.chunk else w.T
+    max_tokens = chunk if chunk else w.T
     ctx = moe.MoeLayer(w.d, w.E, w.I, w.k, max_tokens, x_dtype=moe.MOE_F32 if w.x_dtype == "f32" else moe.MOE_BF16,
                        has_router_bias=w.skewed, has_shared=w.I_s > 0, shared_gate=args.shared_gate)
-    if args.chunk:  # chunked prefill: workspace for `chunk` tokens, the layer over all T in slices
-        moe.moe_set_chunk_tokens(ctx.ctx, args.chunk)
+    if chunk:  # chunked prefill: workspace for `chunk` tokens, the layer over all T in slices
+        moe.moe_set_chunk_tokens(ctx.ctx, chunk)
     path = moe.MOE_PATH_AUTO if args.path == "auto" else (moe.MOE_PATH_GEMV if args.path == "gemv"
                                                           else moe.MOE_PATH_GEMM)
     moe.moe_set_path(ctx.ctx, path)
@@ -331,7 +366,7 @@ def run_ours(args, rank, world, dev):
     whole_layer = eff_path == moe.MOE_PATH_GEMV  # the dominant kernel is the whole layer
     # the configuration a traffic record must have been taken on (per-launch traffic
     # does not depend on the number of stacked layers)
-    traffic_key = w.name + ("+shared_gate" if args.shared_gate else "") + (f"+chunk{args.chunk}" if args.chunk else "")
+    traffic_key = w.name + ("+shared_gate" if args.shared_gate else "") + (f"+chunk{chunk}" if chunk else "")
     if layers > 1:
         # stacked layers with fixed weights: a layer's blocks may start on its
         # weights while the previous layer's kernel finishes (moe_set_overlap)
@@ -363,7 +398,7 @@ def run_ours(args, rank, world, dev):
     with torch.cuda.stream(stream):
         for L in range(layers):
             p = weights[L]
-            step_t = args.chunk or w.T  # moe_route keeps the T <= max_tokens limit: route slice by slice
+            step_t = chunk or w.T  # moe_route keeps the T <= max_tokens limit: route slice by slice
             idx = [ctx.route(xd[L][t0:t0 + step_t], p["router_w"], p["router_b"], stream=stream)["idx"].cpu().numpy()
                    for t0 in range(0, w.T, step_t)]
             costs.append(layer_costs(w, np.concatenate(idx), args.shared_gate))
@@ -465,11 +500,12 @@ def run_ours(args, rank, world, dev):
         roof["traffic"] = profiled_traffic("grouped_gemm_kernel<gate_up>", traffic_key)
         roof.update(kernel="grouped_gemm_kernel<gate_up>", algorithmic_bytes_per_launch=int(per_launch_b),
                     algorithmic_flops_per_launch=int(per_launch_f), avg_launch_us=round(kern_avg_ms * 1e3, 2),
-                    tensor_frac=round(tc_frac, 4), hbm_frac=round(hbm_frac, 4), peak_source=peaks["source"])
+                    tensor_frac=round(tc_frac, 4), hbm_frac=round(hbm_frac, 4), peak_source=peaks["source"],
+                    _hbm_peak=peaks["hbm_gbs"], _tc_peak=peaks["bf16_tflops"])
     layer_bytes = statistics.mean(c["layer_bytes"] for c in costs)
     layer_flops = statistics.mean(c["layer_flops"] for c in costs)
     ms_layer = ms_step / layers
-    if args.chunk and args.chunk < w.T:
+    if chunk and chunk < w.T:
         # chunked: the event hook times one slice's launch, not the layer's; report the
         # whole layer against the layer's minimum bytes (weights read once), which the
         # chunked run exceeds by design (the selected experts are read once per slice)
@@ -477,9 +513,13 @@ def run_ours(args, rank, world, dev):
         roof = dict(bound="hbm", achieved=round(gbs, 1), peak=peaks["hbm_gbs"], unit="GB/s",
                     frac=round(gbs / peaks["hbm_gbs"], 4), traffic=None, kernel="whole layer, chunked",
                     algorithmic_bytes_per_launch=int(layer_bytes), peak_source=peaks["source"])
+    roof = with_nominal(roof)
     whole = dict(ms_per_layer=round(ms_layer, 5),
                  hbm_frac_of_layer=round(layer_bytes / (ms_layer / 1e3) / 1e9 / peaks["hbm_gbs"], 4),
                  tensor_frac_of_layer=round(layer_flops / (ms_layer / 1e3) / 1e12 / peaks["bf16_tflops"], 4),
+                 hbm_frac_of_layer_nominal=round(layer_bytes / (ms_layer / 1e3) / 1e9 / NOMINAL["hbm_gbs"], 4),
+                 tensor_frac_of_layer_nominal=round(layer_flops / (ms_layer / 1e3) / 1e12 / NOMINAL["bf16_tflops"],
+                                                    4),
                  algorithmic_bytes_per_layer=int(layer_bytes), algorithmic_flops_per_layer=int(layer_flops),
                  distinct_experts_per_layer=round(statistics.mean(c["distinct"] for c in costs), 1))
 
@@ -488,7 +528,7 @@ def run_ours(args, rank, world, dev):
         cpu = None
         if not args.no_cpu_baseline and world == 1:
             hosts = [host_layer_for_oracle(w, L, weights[L], xh[L]) for L in range(layers)]
-            v, n, el, thr = oracle_sample(w, args.cpu_seconds, hosts)
+            v, n, el, thr = oracle_sample(w, cpu_seconds, hosts)
             cpu = dict(value=round(v, 3), unit=UNIT, cores=thr, kind="oracle",
                        sample=f"{n} token-layers (8 random tokens per layer, all {layers} layers, repeated) "
                               f"in {el:.1f} s; fp64 numpy, BLAS threads = {thr}")
@@ -503,7 +543,7 @@ def run_ours(args, rank, world, dev):
                                    if layer_bytes * layers > L2_BYTES else
                                    f"inputs fit in L2 ({layer_bytes * layers / 1e6:.0f} MB per step): "
                                    f"a profiling run, not a bench number"),
-                               parallelism=f"replicas x{world}", **({"chunk_tokens": args.chunk} if args.chunk else {}),
+                               parallelism=f"replicas x{world}", **({"chunk_tokens": chunk} if chunk else {}),
                                **({"shared_gate": "sigmoid"} if args.shared_gate else {})),
                    e2e=dict(value=round(e2e_value, 1), unit=UNIT,
                             h2d_bytes_per_step=int(sum(t.numel() * t.element_size() for t in xh)),
@@ -511,6 +551,16 @@ def run_ours(args, rank, world, dev):
                    gpu_launches=int(launches), roofline=roof, layer=whole, clocks=clk, cpu_baseline=cpu)
     ctx.close()
     return out
+
+
+NESTED_PREFILL = ("prefill_balanced", "prefill_skewed")
+
+
+def nested(sub):
+    """The per-workload part of a JSON line, for nesting inside the main line."""
+    keep = ("value", "unit", "steps", "warmup", "ms_per_step", "config", "e2e", "gpu_launches", "roofline", "layer",
+            "clocks", "cpu_baseline")
+    return {k: sub[k] for k in keep if k in sub}
 
 
 def run_reference(args):
@@ -564,6 +614,10 @@ def main():
                     help="stacked layers per step (default: the workload's own; fewer only for small profiling runs)")
     ap.add_argument("--shared-gate", action="store_true",
                     help="the sigmoid-gated shared-expert variant (a gate row appended to the router)")
+    ap.add_argument("--no-prefill", action="store_true",
+                    help="decode only: skip the nested prefill_balanced / prefill_skewed measurements")
+    ap.add_argument("--prefill-cpu-seconds", type=float, default=6.0,
+                    help="oracle time budget of each nested prefill measurement's cpu_baseline")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -583,6 +637,15 @@ def main():
         torch.cuda.set_device(dev)
         torch.distributed.init_process_group("nccl", device_id=dev)
     out = run_ours(args, rank, world, dev)
+    if args.workload == "decode" and not args.no_prefill:
+        # the metric's second half: the T = 4096 prefill layer, balanced and
+        # skewed routing, each measured the same way and nested in the line
+        torch.cuda.empty_cache()
+        for name in NESTED_PREFILL:
+            sub = run_ours(args, rank, world, dev, workload=name, cpu_seconds=args.prefill_cpu_seconds, chunk=0)
+            torch.cuda.empty_cache()
+            if rank == 0:
+                out[name] = nested(sub)
     if rank == 0:
         print(json.dumps(out), flush=True)
     if world > 1:

@@ -70,6 +70,8 @@ def lib() -> ctypes.CDLL:
         L.moe_launch_count.restype = ctypes.c_longlong
         L.moe_decode_noalloc.argtypes = [P, I, I, I, I, I, I, P, P, P, P, P, P, P, P]
         L.moe_decode_noalloc.restype = I
+        L.moe_last_routing.argtypes = [P, P, P, P, P, P, P, ctypes.POINTER(I), ctypes.POINTER(I), P]
+        L.moe_last_routing.restype = I
         L.moe_status.argtypes = [P]
         L.moe_strerror.argtypes = [I]
         L.moe_strerror.restype = ctypes.c_char_p
@@ -209,11 +211,33 @@ def moe_forward(ctx, x, router_w, router_b, experts_gate_up, experts_down, share
                              _ptr(experts_down), _ptr(shared_w), top_k, _ptr(y), _stream(stream)), "moe_forward")
 
 
+def moe_last_routing(ctx, n_experts, stream=None) -> dict:
+    """The routing tables the last ``moe_forward`` on ``ctx`` computed and used
+    (idx, w, counts, offsets, perm, slot), as device tensors; see moe.h."""
+    import torch
+
+    T, k = ctypes.c_int(), ctypes.c_int()
+    _check(lib().moe_last_routing(ctx, None, None, None, None, None, None, ctypes.byref(T), ctypes.byref(k), None),
+           "moe_last_routing")
+    T, k = T.value, k.value
+    dev = torch.device("cuda", torch.cuda.current_device())
+    out = dict(idx=torch.empty(T, k, dtype=torch.int32, device=dev), w=torch.empty(T, k, dtype=torch.float32, device=dev),
+               counts=torch.empty(n_experts, dtype=torch.int32, device=dev),
+               offsets=torch.empty(n_experts + 1, dtype=torch.int32, device=dev),
+               perm=torch.empty(T * k, dtype=torch.int32, device=dev),
+               slot=torch.empty(T, k, dtype=torch.int32, device=dev))
+    _check(lib().moe_last_routing(ctx, _ptr(out["idx"]), _ptr(out["w"]), _ptr(out["counts"]), _ptr(out["offsets"]),
+                                  _ptr(out["perm"]), _ptr(out["slot"]), None, None, _stream(stream)),
+           "moe_last_routing")
+    return out
+
+
 def moe_decode_noalloc(x, router_w, router_b, experts_gate_up, experts_down, shared_w, top_k, y, status=None,
                        stream=None) -> None:
-    """The small-T layer without a context: for callers that cannot allocate
-    device memory (inside a stream capture, or under a no-allocation policy).
-    Scratch memory is a fixed device array inside the library; see moe.h."""
+    """The small-T layer without a context, for callers that cannot allocate
+    device memory (a plugin whose host owns every device buffer, a serving loop
+    that must not risk an allocation's device synchronisation).  Scratch memory
+    is a fixed device array inside the library; see moe.h."""
     import torch
 
     for name, t, dt in (("x", x, None), ("router_w", router_w, torch.float32), ("router_b", router_b, torch.float32),
@@ -265,6 +289,10 @@ class MoeLayer:
                    perm=torch.empty(T * k, dtype=torch.int32, device=dev))
         moe_route(self.ctx, x, router_w, router_b, k, stream=stream, **out)
         return out
+
+    def last_routing(self, stream=None) -> dict:
+        """Routing tables of the last ``forward`` (device tensors)."""
+        return moe_last_routing(self.ctx, self.n_experts, stream)
 
     def status(self) -> int:
         return moe_status(self.ctx)

@@ -36,6 +36,8 @@ struct moe_ctx {
   int timed_kernel = -1;
   cudaEvent_t ev_start = nullptr, ev_stop = nullptr;
   long long launches = 0;
+  // T and top_k of the last moe_forward call (or slice) whose routing tables the scratch holds
+  int last_T = 0, last_k = 0;
 };
 
 namespace {
@@ -401,12 +403,34 @@ int moe_route(moe_ctx* ctx, const void* x, int T, const float* router_w, const f
     if ((rc = make_map(ctx, &maps.wr_split, ctx->sc.wr_split, s.d, 3 * s.E, 64, 256)) != MOE_OK) return rc;
   }
   if ((rc = run_route(ctx, s, x, router_w, router_b, tensor, &maps, st)) != MOE_OK) return rc;
-  return cuda_fail(launch_export_route(s, ctx->sc, idx, w, counts, offsets, perm, st));
+  ctx->last_T = 0;  // the scratch tables now hold this call's routing, not a forward's
+  return cuda_fail(launch_export_route(s, ctx->sc, idx, w, counts, offsets, perm, nullptr, st));
+}
+
+int moe_last_routing(moe_ctx* ctx, int32_t* idx, float* w, int32_t* counts, int32_t* offsets, int32_t* perm,
+                     int32_t* slot, int* T_out, int* k_out, void* stream) {
+  if (!ctx || ctx->last_T <= 0) return MOE_ERR_ARG;
+  if ((idx && !aligned16(idx)) || (w && !aligned16(w)) || (counts && !aligned16(counts)) ||
+      (offsets && !aligned16(offsets)) || (perm && !aligned16(perm)) || (slot && !aligned16(slot)))
+    return MOE_ERR_ALIGN;
+  if (T_out) *T_out = ctx->last_T;
+  if (k_out) *k_out = ctx->last_k;
+  const Shapes s = shapes(ctx, ctx->last_T, ctx->last_k);
+  return cuda_fail(launch_export_route(s, ctx->sc, idx, w, counts, offsets, perm, slot,
+                                       static_cast<cudaStream_t>(stream)));
 }
 
 static int forward_one(moe_ctx* ctx, const void* x, int T, const float* router_w, const float* router_b,
                        const void* experts_gate_up, const void* experts_down, const void* shared_w, int top_k,
                        void* y, void* stream);
+
+// After a forward call: the scratch routing tables are that call's (for
+// moe_last_routing) if it launched its kernels.
+static int remember_routing(moe_ctx* ctx, int T, int top_k, int rc) {
+  ctx->last_T = rc == MOE_OK ? T : 0;
+  ctx->last_k = rc == MOE_OK ? top_k : 0;
+  return rc;
+}
 
 int moe_set_chunk_tokens(moe_ctx* ctx, int chunk) {
   if (!ctx || chunk < 0 || chunk > ctx->cfg.max_tokens) return MOE_ERR_ARG;
@@ -468,7 +492,7 @@ static int forward_one(moe_ctx* ctx, const void* x, int T, const float* router_w
     });
     ctx->next_wr = nullptr;  // a hint serves one call
     ctx->next_shared = nullptr;
-    return cuda_fail(err);
+    return remember_routing(ctx, T, top_k, cuda_fail(err));
   }
   if (path == MOE_PATH_GEMV) {
     if ((rc = run_route(ctx, s, x, router_w, router_b, false, nullptr, st)) != MOE_OK) return rc;
@@ -478,7 +502,7 @@ static int forward_one(moe_ctx* ctx, const void* x, int T, const float* router_w
         launch(ctx, MOE_K_GEMV_GATE_UP, st, [&] { return launch_gemv_gate_up(s, x, gu, sw, sc, ctl, sms, st); });
     if (err == cudaSuccess)
       err = launch(ctx, MOE_K_GEMV_DOWN, st, [&] { return launch_gemv_down(s, dn, sw, y, sc, ctl, sms, st); });
-    return cuda_fail(err);
+    return remember_routing(ctx, T, top_k, cuda_fail(err));
   }
 
   // grouped-GEMM path
@@ -506,7 +530,7 @@ static int forward_one(moe_ctx* ctx, const void* x, int T, const float* router_w
   if (err == cudaSuccess)
     err = launch(ctx, MOE_K_GEMM_DOWN, st, [&] { return launch_gemm_down(s, maps, sc, ctl, sms, st); });
   if (err == cudaSuccess) err = launch(ctx, MOE_K_COMBINE, st, [&] { return launch_combine(s, y, sc, st); });
-  return cuda_fail(err);
+  return remember_routing(ctx, T, top_k, cuda_fail(err));
 }
 
 int moe_status(moe_ctx* ctx) {

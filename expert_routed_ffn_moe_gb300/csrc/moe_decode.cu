@@ -166,15 +166,16 @@ cudaError_t launch_decode_fused(const Shapes& s, const void* x, const float* wr,
 // Allocation-free variant of the fused decode layer (moe_decode_noalloc).
 //
 // Some callers cannot call cudaMalloc, so they cannot create a context with
-// moe_init: code that builds its GPU work inside an ongoing CUDA stream capture
-// (allocation is not allowed there), and processes that run under a strict
-// no-allocation policy (real-time serving loops, or hosts whose device memory
-// is owned by another allocator).  For them the same kernel runs on scratch
-// memory that is part of the library image: one file-scope device array, sized
-// for the limits below, that every GPU loading the library holds until exit.
-// The host learns its device address once per device with
-// cudaGetSymbolAddress; the array's name in host code is only a host-side
-// stand-in, never a device address.
+// moe_init: a plugin running inside a host application whose device memory
+// belongs to the host's own allocator (the host hands out every buffer and
+// forbids allocations outside its pool), and serving loops with a fixed
+// latency budget, where an allocation may synchronise the device and stall
+// every stream.  For them the same kernel runs on scratch memory that is part
+// of the library image: one file-scope device array, sized for the limits
+// below, that every GPU loading the library holds until exit.  The host
+// learns its device address once per device with cudaGetSymbolAddress; the
+// array's name in host code is only a host-side stand-in, never a device
+// address.
 // ---------------------------------------------------------------------------
 
 using namespace moe;
@@ -192,7 +193,7 @@ constexpr size_t kNoAllocOffLogits = kNoAllocH;
 constexpr size_t kNoAllocOffIdx = kNoAllocOffLogits + kNoAllocLogits;
 constexpr size_t kNoAllocOffW = kNoAllocOffIdx + kNoAllocPicks;
 constexpr size_t kNoAllocOffStatus = kNoAllocOffW + kNoAllocPicks;
-constexpr size_t kNoAllocOffBar = kNoAllocOffStatus + 256;  // epoch of the last launch
+constexpr size_t kNoAllocOffBar = kNoAllocOffStatus + 256;  // control words: the 64-bit epoch counter
 constexpr size_t kNoAllocBarBytes = 256;
 constexpr size_t kNoAllocBytes = kNoAllocOffBar + kNoAllocBarBytes;
 
@@ -207,11 +208,13 @@ std::mutex g_noalloc_mu;
 
 }  // namespace
 
-// The scratch array (about 1.3 MB).  Every call shares it and it keeps the
-// last call's contents.  Its zero initial contents are a valid start: tag 0
-// is never a launch's epoch, and nothing must be cleared between calls (the
-// epoch word is kept, since a tag left by an earlier call must never match a
-// later one).
+// The scratch array (1,312,256 bytes, about 1.3 MB: tagged h rows 1.18 MB,
+// tagged logits 128 KB, picks, status and control words).  Every call shares
+// it and it keeps the last call's contents.  Its zero initial contents are a
+// valid start: tag 0 is never a launch's epoch, and nothing must be cleared
+// between calls (the epoch counter is kept, since a tag left by an earlier
+// call must never match a later one).
+static_assert(kNoAllocBytes == 1312256, "the documented size of the allocation-free scratch array");
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocBytes];
 
 extern "C" int moe_decode_noalloc(const void* x, int T, int x_dtype, int d, int n_experts, int inter, int top_k,

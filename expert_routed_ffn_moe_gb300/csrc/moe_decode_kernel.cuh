@@ -42,9 +42,9 @@
 // starts on the logits one L2 round trip after the last of them lands, instead
 // of after a barrier's arrive, poll and release and then a separate load.
 // (Per-block "h written" flags behind a fence measured slower: the fence waits
-// out the block's in-flight traffic.)  Every block stores the launch's epoch
-// as it leaves; the next launch, a graph replay included, tags with the one
-// after it.
+// out the block's in-flight traffic.)  Every block publishes the launch's
+// epoch (an atomic maximum on a 64-bit counter) as it leaves; the next launch,
+// a graph replay included, tags with the one after it.
 #pragma once
 #include <math.h>
 
@@ -70,9 +70,9 @@ MOE_DEV void prefetch_l2(const void* p, uint32_t bytes) {
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(p)), "r"(bytes)
                : "memory");
 }
-MOE_DEV unsigned ld_relaxed(const unsigned* p) {
-  unsigned v;
-  asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+MOE_DEV unsigned long long ld_relaxed64(const unsigned long long* p) {
+  unsigned long long v;
+  asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
   return v;
 }
 
@@ -132,7 +132,7 @@ struct DecodeArgs {
   void* y;
   Scratch sc;
   DevCtl ctl;
-  unsigned* bar;   // [1]: epoch of the last launch ([0] unused)
+  unsigned* bar;   // control words: [2..3] the largest epoch published so far (64-bit), [0..1] unused
   // optional prefetch hint: weights the next layer reads first (may be null)
   const float* next_wr;
   const uint16_t* next_shared;
@@ -140,6 +140,10 @@ struct DecodeArgs {
   int slot_bytes;     // bytes per slot: max(gate + up row, chunk_experts down rows)
   int chunk_experts;  // down-projection rows (one per active expert) per slot
 };
+
+// The 64-bit epoch counter of the fused decode kernel inside its control
+// words (bytes 8..15; the block of words is 256-byte aligned).
+MOE_DEV unsigned long long* epoch_word(unsigned* bar) { return reinterpret_cast<unsigned long long*>(bar + 2); }
 
 MOE_DEV void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar, uint64_t policy) {
   asm volatile(
@@ -260,6 +264,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const DecodeA
   __shared__ uint8_t pair_t[MAXT > 1 ? MAXT * (kMaxTopK + 1) : 1];
   __shared__ int n_act_s, flag_s;
   __shared__ unsigned ep_s;  // this launch's epoch: the tag of every value it publishes
+  __shared__ unsigned long long ep64_s;  // the same epoch as a 64-bit count (never wraps)
   __shared__ int warp_tot[kWarps];
   __shared__ __align__(8) uint64_t full[kMaxSlots];  // ring slot filled (TMA transaction count)
   __shared__ int slot_issued[kMaxSlots];             // items issued into each slot so far
@@ -310,8 +315,12 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const DecodeA
     // scratch (a no-op for a normal launch).
     asm volatile("griddepcontrol.wait;" ::: "memory");
     if (tid == 0) {
-      const unsigned e = ld_relaxed(A.bar + 1) + 1u;  // the previous launch's epoch + 1 (0 is never a tag)
-      ep_s = e ? e : 1u;
+      // the largest epoch any earlier launch used, + 1; the tag is its low 32
+      // bits, skipping 0 (zeroed scratch must never look ready)
+      unsigned long long e = ld_relaxed64(epoch_word(A.bar)) + 1ull;
+      if ((unsigned)e == 0u) ++e;
+      ep64_s = e;
+      ep_s = (unsigned)e;
     }
     const int nx = s.T * s.d;
     if (XBF16) {
@@ -513,6 +522,21 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const DecodeA
       int base = 0;
       for (int i = 0; i < warp; ++i) base += warp_tot[i];
       const int excl = base + incl - v;
+      if (b == 0 && sc.counts != nullptr && tid < s.E) {
+        // the layer's grouping tables, for moe_last_routing: block 0 writes its
+        // in-shared-memory grouping out once (counts, exclusive offsets, the
+        // stable permutation and each pick's position in it)
+        sc.counts[tid] = cnt;
+        sc.offsets[tid] = excl & 0xffff;
+        for (int t = 0, i = 0; t < s.T; ++t)
+          if ((m >> t) & 1u) {
+            const int p = (excl & 0xffff) + i++;
+            sc.perm[p] = t;
+            for (int j = 0; j < s.k; ++j)
+              if (sel_e[t][j] == tid) sc.slot[(size_t)t * s.k + j] = p;
+          }
+        if (tid == 0) sc.offsets[s.E] = tk;
+      }
       if (flag) {
         const int pos = excl >> 16;
         act_e[pos] = tid;
@@ -570,6 +594,23 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const DecodeA
     if (warp == 0 && lane < S && n_sh + lane < n_items) {
       fence_proxy_async_smem();  // after the phase-A reads of the slots, before the copies overwrite them
       issue_item(A, n_sh + lane, (n_sh + lane) % S, n_sh, nu, nch, b, G, n_act, act_e, ring, full, slot_issued);
+    }
+    if (MAXT == 1 && b == 0 && sc.counts != nullptr && tid >= 32 && tid < 32 + s.E) {
+      // batch 1: the layer's grouping tables, for moe_last_routing (one row per
+      // pick, in ascending expert id); warps 1.. write them while warp 0 issues
+      const int e = tid - 32;
+      int c = 0, o = 0;
+      for (int j = 0; j < s.k; ++j) {
+        c += sel_e[0][j] == e;
+        o += sel_e[0][j] < e;
+      }
+      sc.counts[e] = c;
+      sc.offsets[e] = o;
+      if (e < s.k) {
+        sc.perm[e] = 0;
+        sc.slot[e] = e;
+      }
+      if (e == 0) sc.offsets[s.E] = s.k;
     }
     // routed gate/up GEMV + SwiGLU: routed unit j (item n_sh + j) goes to warp j mod kWarps
     for (int j = warp; j < nu; j += kWarps) {
@@ -791,12 +832,23 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const DecodeA
   __syncthreads();
   if (flag_s == 0 && tid < A.ring_slots) drain_slot(full, slot_issued, tid, A.ctl);
   // leave: publish this launch's epoch (the next launch, which starts after
-  // this grid completes, tags with epoch + 1).  Every block stores the same
-  // value, with no exit counter: no block can leave before every block has
-  // read the old epoch, since each first waits for every block's logits,
-  // which carry it (a block that gives up does so only after the spin limit,
-  // long after all blocks of the cooperative launch have started).
-  if (tid == 0) A.bar[1] = ep_s;
+  // this grid completes, tags with one more than the largest epoch published).
+  // Every block publishes, with no exit counter: in a run without timeouts no
+  // block can leave before every block has read the old epoch, since each
+  // first waits for every block's logits, which carry it.  A block that gave
+  // up may have left before a late block read the word (which then took
+  // epoch + 1); so a block that gave up publishes with an atomic maximum,
+  // which no other store can lower.  A block that finished normally saw every
+  // block's logits tagged with its own epoch, so in its launch all blocks
+  // share one epoch and its plain store writes that same value (and costs no
+  // atomic round trip on the common path).  Either way the next launch's
+  // epoch exceeds every tag written so far.
+  if (tid == 0) {
+    if (flag_s == 0)
+      atomicMax(epoch_word(A.bar), ep64_s);
+    else
+      *reinterpret_cast<volatile unsigned long long*>(epoch_word(A.bar)) = ep64_s;
+  }
 }
 
 

@@ -43,7 +43,7 @@ struct Scratch {
   float* h_gemv;          // [Tg*k + Tg, I] fp32 SwiGLU activations (GEMV path)
   uint16_t* out;          // [T*k + T, d] bf16 expert outputs, grouped rows (GEMM path)
   unsigned* status;       // device status word
-  unsigned* gridbar;      // fused decode kernel: [1] epoch of the last launch
+  unsigned* gridbar;      // fused decode kernel: control words, [2..3] = 64-bit epoch counter
   float* dec_logits;      // fused decode kernel: [dec_reps][T][E] router logits as (fp32, epoch) 64-bit words
   float* dec_h;           // fused decode kernel: [dec_hreps][T*k + T][I] SwiGLU activations as (fp32, epoch) words
   float* sgate;           // [T] sigmoid(x_t . g), the shared expert's gate (GEMV and GEMM paths)
@@ -72,7 +72,7 @@ cudaError_t launch_select(const Shapes& s, const float* rb, int logit_parts, con
 cudaError_t launch_group(const Shapes& s, const Scratch& sc, const DevCtl& ctl, cudaStream_t st,
                          const void* x_rows = nullptr);
 cudaError_t launch_export_route(const Shapes& s, const Scratch& sc, int32_t* idx, float* w, int32_t* counts,
-                                int32_t* offsets, int32_t* perm, cudaStream_t st);
+                                int32_t* offsets, int32_t* perm, int32_t* slot, cudaStream_t st);
 
 // moe_gemv.cu
 size_t gemv_gate_up_smem(const Shapes& s);

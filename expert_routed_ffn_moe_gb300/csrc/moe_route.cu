@@ -456,7 +456,7 @@ cudaError_t launch_group(const Shapes& s, const Scratch& sc, const DevCtl& ctl, 
 }
 
 cudaError_t launch_export_route(const Shapes& s, const Scratch& sc, int32_t* idx, float* w, int32_t* counts,
-                                int32_t* offsets, int32_t* perm, cudaStream_t st) {
+                                int32_t* offsets, int32_t* perm, int32_t* slot, cudaStream_t st) {
   const size_t tk = (size_t)s.T * s.k;
   cudaError_t err = cudaSuccess;
   if (idx && err == cudaSuccess) err = cudaMemcpyAsync(idx, sc.idx, tk * 4, cudaMemcpyDeviceToDevice, st);
@@ -466,6 +466,7 @@ cudaError_t launch_export_route(const Shapes& s, const Scratch& sc, int32_t* idx
   if (offsets && err == cudaSuccess)
     err = cudaMemcpyAsync(offsets, sc.offsets, (size_t)(s.E + 1) * 4, cudaMemcpyDeviceToDevice, st);
   if (perm && err == cudaSuccess) err = cudaMemcpyAsync(perm, sc.perm, tk * 4, cudaMemcpyDeviceToDevice, st);
+  if (slot && err == cudaSuccess) err = cudaMemcpyAsync(slot, sc.slot, tk * 4, cudaMemcpyDeviceToDevice, st);
   return err;
 }
 

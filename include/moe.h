@@ -220,21 +220,25 @@ long long moe_launch_count(moe_ctx* ctx);
 int moe_inject_stall(moe_ctx* ctx, int on);
 
 /* Allocation-free decode layer (no counterpart in the source pages; added for
- * callers that cannot allocate device memory).  Code that records its GPU work
- * inside an ongoing CUDA stream capture cannot call cudaMalloc there, and
- * processes under a strict no-allocation policy (real-time serving loops,
- * hosts whose device memory belongs to another allocator) must not; neither can
- * create a context with moe_init.  This entry point runs the same fused decode
- * kernel as moe_forward's small-T path, but its scratch memory is a fixed
- * device array inside the library (about 600 KB, held on every GPU that loads
- * the library until the process exits).  It calls no cudaMalloc, cudaFree or
- * allocating library routine.
+ * callers that cannot allocate device memory).  A plugin running inside a host
+ * application whose device memory belongs to the host's own allocator (every
+ * buffer comes from the host's pool; allocating outside it is forbidden), or a
+ * serving loop with a fixed latency budget (an allocation may synchronise the
+ * device and stall every stream), cannot call cudaMalloc, and so cannot create
+ * a context with moe_init.  This entry point runs the same fused decode kernel
+ * as moe_forward's small-T path, but its scratch memory is a fixed device array
+ * inside the library (1,312,256 bytes, about 1.3 MB, held on every GPU that
+ * loads the library until the process exits).  It calls no cudaMalloc, cudaFree
+ * or allocating library routine.
  *
  * Inputs and outputs are as for moe_forward, with the shapes passed directly:
  * x [T, d] (x_dtype), router_w [E, d] fp32, router_b [E] fp32 or NULL,
  * experts_gate_up [E, 2*inter, d] bf16, experts_down [E, d, inter] bf16,
  * shared_w (shared gate_up [2*inter, d] then down [d, inter], bf16) or NULL,
- * y [T, d] (x_dtype).  status: optional device word (NULL = none) into which a
+ * y [T, d] (x_dtype).  The two moe_config variants are fixed: a router bias, if
+ * given, enters both the selection and the weights (bias_select_only = 0), and
+ * the shared expert, if given, has weight one (shared_gate = 0).
+ * status: optional device word (NULL = none) into which a
  * kernel ORs a failure it detects (1 = a bounded wait ran out, 2 = an index was
  * out of range); it is not cleared by the call.
  * Limits of the fixed scratch: T <= 16, top_k <= 8, inter <= 1024, E <= 256,
@@ -250,6 +254,21 @@ int moe_inject_stall(moe_ctx* ctx, int on);
 int moe_decode_noalloc(const void* x, int T, int x_dtype, int d, int n_experts, int inter, int top_k,
                        const float* router_w, const float* router_b, const void* experts_gate_up,
                        const void* experts_down, const void* shared_w, void* y, unsigned* status, void* stream);
+
+/* Test and inspection hook: copy the routing tables that the last moe_forward
+ * call on `ctx` computed and used itself (for a chunked call: its last slice),
+ * device to device, asynchronously on `stream`.  T and top_k are that call's.
+ * Outputs (caller-owned device buffers, any may be NULL to skip it): idx
+ * [T, top_k] int32 (ascending expert id per row), w [T, top_k] fp32, counts [E]
+ * int32, offsets [E + 1] int32, perm [T * top_k] int32 (token ids grouped by
+ * expert, ascending within a group), slot [T, top_k] int32 (the position in
+ * perm of each (token, pick)).  Every path writes all six: the grouped GEMMs and
+ * the GEMV kernels through the grouping kernels, the fused small-T kernel from
+ * its first block's in-kernel grouping.  *T_out / *k_out (host pointers, may be
+ * NULL) receive that call's T and top_k.  MOE_ERR_ARG if ctx is NULL or no
+ * moe_forward call has run on it yet; MOE_ERR_ALIGN for unaligned outputs. */
+int moe_last_routing(moe_ctx* ctx, int32_t* idx, float* w, int32_t* counts, int32_t* offsets, int32_t* perm,
+                     int32_t* slot, int* T_out, int* k_out, void* stream);
 
 /* Static description of a return code. */
 const char* moe_strerror(int code);

@@ -49,15 +49,19 @@ def make_layer(w: mw.Workload, max_tokens=None, path=moe.MOE_PATH_AUTO, router=m
     return layer
 
 
-def gpu_run(w, inp, layer, dev_in=None, top_k=None):
+def gpu_run(w, inp, layer, dev_in=None, top_k=None, with_forward_tables=False):
+    """moe_route's tables and y from moe_forward; with ``with_forward_tables``
+    also the tables moe_forward itself computed (read back with moe_last_routing)."""
     d = dev_in or device_inputs(w, inp)
     k = top_k or w.k
     r = layer.route(d["x"], d["router_w"], d["router_b"], top_k=k)
+    r = {key: v.cpu().numpy() for key, v in r.items()}
     y = layer.forward(d["x"], d["router_w"], d["router_b"], d["gate_up"], d["down"], d["shared"], top_k=k)
+    fwd = {key: v.cpu().numpy() for key, v in layer.last_routing().items()}
     torch.cuda.synchronize()
     status = layer.status()
     assert status == moe.MOE_OK, moe.moe_strerror(status)
-    return {key: v.cpu().numpy() for key, v in r.items()}, y
+    return (r, y, fwd) if with_forward_tables else (r, y)
 
 
 def oracle_routing(w, inp, k=None, bias_select_only=False):
@@ -71,13 +75,17 @@ def oracle_routing(w, inp, k=None, bias_select_only=False):
     return dict(idx=idx, w=wts, margin=margin, counts=counts, offsets=offsets, perm=perm, slot=slot)
 
 
-def check_routing(got, ref):
-    assert np.array_equal(got["idx"], ref["idx"]), "routing indices differ"
-    assert np.array_equal(got["counts"], ref["counts"]), "per-expert counts differ"
-    assert np.array_equal(got["offsets"], ref["offsets"]), "expert offsets differ"
-    assert np.array_equal(got["perm"], ref["perm"]), "permutation differs"
+def check_routing(got, ref, what="moe_route"):
+    """Bit-exact idx, counts, offsets, perm (and slot when ``got`` has it);
+    weights within W_REL relative."""
+    assert np.array_equal(got["idx"], ref["idx"]), f"{what}: routing indices differ"
+    assert np.array_equal(got["counts"], ref["counts"]), f"{what}: per-expert counts differ"
+    assert np.array_equal(got["offsets"], ref["offsets"]), f"{what}: expert offsets differ"
+    assert np.array_equal(got["perm"], ref["perm"]), f"{what}: permutation differs"
+    if "slot" in got:
+        assert np.array_equal(got["slot"], ref["slot"]), f"{what}: slots differ"
     err = np.abs(got["w"] - ref["w"])
-    assert np.all(err <= W_REL * ref["w"] + 1e-7), f"routing weights differ (max {err.max():.3e})"
+    assert np.all(err <= W_REL * ref["w"] + 1e-7), f"{what}: routing weights differ (max {err.max():.3e})"
 
 
 def oracle_y(w, inp, tokens, k=None, bias_select_only=False, shared_gate_w=None):
@@ -97,6 +105,39 @@ def check_y(got: np.ndarray, ref: np.ndarray, what=""):
     return rel, mx
 
 
+def tile_position_tokens(ref, T: int, n: int, bm: int = 128, seed: int = 0) -> np.ndarray:
+    """At least ``n`` tokens (all if T <= n) that cover every grouped-GEMM m-tile
+    position: for each expert group (``ref`` = oracle routing) the first, second
+    and last rows of its first, second and last tiles of ``bm`` rows, the same
+    for the shared expert's group (all T tokens in order), the first and last
+    token, then random tokens up to ``n``."""
+    if T <= n:
+        return np.arange(T)
+    pick = {0, T - 1}
+    offsets, perm = ref["offsets"], ref["perm"]
+    for e in range(len(offsets) - 1):
+        lo, hi = int(offsets[e]), int(offsets[e + 1])
+        c = hi - lo
+        if c == 0:
+            continue
+        n_tiles = (c + bm - 1) // bm
+        for tile in {0, 1, n_tiles - 1}:
+            if tile >= n_tiles:
+                continue
+            r0, r1 = tile * bm, min(c, (tile + 1) * bm)
+            for r in {r0, r0 + 1, r1 - 1}:
+                if r0 <= r < r1:
+                    pick.add(int(perm[lo + r]))
+    for t0 in (0, bm, T - T % bm if T % bm else T - bm):
+        for t in (t0, t0 + 1, min(T, t0 + bm) - 1):
+            if 0 <= t < T:
+                pick.add(t)
+    rng = np.random.default_rng(seed)
+    while len(pick) < n:
+        pick.update(rng.choice(T, n - len(pick), replace=False).tolist())
+    return np.array(sorted(pick))
+
+
 def sample_tokens(T: int, n: int, seed: int = 0) -> np.ndarray:
     """All tokens if T <= n, else n tokens spread over the range incl. both ends."""
     if T <= n:
@@ -111,4 +152,4 @@ def y_host(y: torch.Tensor) -> np.ndarray:
 
 
 __all__ = ["bf16_dev", "device_inputs", "make_layer", "gpu_run", "oracle_routing", "check_routing", "oracle_y",
-           "check_y", "sample_tokens", "layer_inputs", "y_host"]
+           "check_y", "sample_tokens", "tile_position_tokens", "layer_inputs", "y_host"]

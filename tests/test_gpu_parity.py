@@ -1,9 +1,12 @@
 """GPU path vs the fp64 oracle, through the C ABI, on the seeded workloads.
 
-Routing (indices, counts, offsets, permutation) must match bit for bit and y
-must be within relative L2 1e-2 / max-abs 2e-2 (tests/moe_case.py).  Full-size
-workloads compare routing for every token and y on a sample of tokens that the
-oracle computes one by one; small ones compare every token.
+Routing (indices, counts, offsets, permutation, slots) must match bit for bit
+and y must be within relative L2 1e-2 / max-abs 2e-2 (tests/moe_case.py).  The
+routing is checked twice: the tables moe_route returns, and the tables
+moe_forward itself computed and used (read back with moe_last_routing).  y is
+compared on every token up to T = 4096; at T = 32768 on 4096 tokens that cover
+the first, second and last rows of the first, second and last m-tile of every
+expert group and of the shared expert's group.
 """
 import dataclasses
 
@@ -14,7 +17,7 @@ import torch
 import moe_workloads as mw
 import expert_routed_ffn_moe_gb300 as moe
 from moe_case import (check_routing, check_y, device_inputs, gpu_run, layer_inputs, make_layer, oracle_routing,
-                      oracle_y, sample_tokens, y_host)
+                      oracle_y, tile_position_tokens, y_host)
 
 pytestmark = pytest.mark.gpu
 
@@ -27,14 +30,15 @@ def custom(name, **kw):
     return mw.Workload(name, **base)
 
 
-def full_case(w, layer_id=0, path=moe.MOE_PATH_AUTO, router=moe.MOE_ROUTER_AUTO, n_sample=64, inp=None):
+def full_case(w, layer_id=0, path=moe.MOE_PATH_AUTO, router=moe.MOE_ROUTER_AUTO, n_sample=4096, inp=None):
     inp = inp or layer_inputs(w, layer_id)
     layer = make_layer(w, path=path, router=router)
-    got, y = gpu_run(w, inp, layer)
+    got, y, fwd = gpu_run(w, inp, layer, with_forward_tables=True)
     layer.close()
     ref = oracle_routing(w, inp)
     check_routing(got, ref)
-    toks = sample_tokens(w.T, n_sample)
+    check_routing(fwd, ref, "moe_forward")
+    toks = tile_position_tokens(ref, w.T, n_sample)
     return check_y(y_host(y)[toks], oracle_y(w, inp, toks), f"{w.name} layer {layer_id}")
 
 
@@ -59,19 +63,19 @@ def test_sweep_small(name):
 
 
 def test_prefill_balanced():
-    full_case(W["prefill_balanced"], n_sample=48)
+    full_case(W["prefill_balanced"])
 
 
 def test_prefill_skewed():
-    full_case(W["prefill_skewed"], n_sample=48)
+    full_case(W["prefill_skewed"])
 
 
 def test_long_prefill_32768():
-    full_case(W["sweep_T32768"], n_sample=24)
+    full_case(W["sweep_T32768"])
 
 
 def test_prefill_simt_router_matches():
-    full_case(W["prefill_balanced"], router=moe.MOE_ROUTER_SIMT, n_sample=16)
+    full_case(W["prefill_balanced"], router=moe.MOE_ROUTER_SIMT)
 
 
 # ------------------------------------------------------------ edge cases
@@ -107,11 +111,12 @@ def test_top_k_below_configured():
     inp = layer_inputs(dataclasses.replace(w, k=2))
     w2 = dataclasses.replace(w, k=2)
     layer = make_layer(w)  # configured for top-8, called with top-2
-    got, y = gpu_run(w2, inp, layer, top_k=2)
+    got, y, fwd = gpu_run(w2, inp, layer, top_k=2, with_forward_tables=True)
     layer.close()
-    check_routing(got, oracle_routing(w2, inp))
-    toks = sample_tokens(w.T, 40)
-    check_y(y_host(y)[toks], oracle_y(w2, inp, toks), "top-2")
+    ref = oracle_routing(w2, inp)
+    check_routing(got, ref)
+    check_routing(fwd, ref, "moe_forward")
+    check_y(y_host(y), oracle_y(w2, inp, np.arange(w.T)), "top-2")
 
 
 def test_many_experts_per_token():
@@ -196,7 +201,7 @@ def test_bounded_wait_reports_timeout_and_context_recovers():
     torch.cuda.synchronize()
     assert layer.status() == moe.MOE_OK
     layer.close()
-    toks = sample_tokens(w.T, 32)
+    toks = np.arange(w.T)
     check_y(y_host(y)[toks], oracle_y(w, inp, toks), "after timeout")
 
 
@@ -298,8 +303,12 @@ def test_chunked_prefill_matches_oracle_and_unchunked():
     small = make_layer(w, max_tokens=256)
     moe.moe_set_chunk_tokens(small.ctx, 256)
     y_chunked = small.forward(d["x"], *args).clone()
+    last = {key: v.cpu().numpy() for key, v in small.last_routing().items()}
     torch.cuda.synchronize()
     assert small.status() == moe.MOE_OK
+    # the tables of the last slice (tokens 512..699) are those of that slice alone
+    tail = dict(inp, x=inp["x"][512:])
+    check_routing(last, oracle_routing(dataclasses.replace(w, T=188), tail), "last slice")
     with pytest.raises(moe.MoeError):
         moe.moe_set_chunk_tokens(small.ctx, 257)  # above max_tokens
     small.close()
@@ -309,7 +318,7 @@ def test_chunked_prefill_matches_oracle_and_unchunked():
     assert full.status() == moe.MOE_OK
     full.close()
     assert torch.equal(y_chunked, y_full)
-    toks = sample_tokens(w.T, 48)
+    toks = np.arange(w.T)
     check_y(y_host(y_chunked)[toks], oracle_y(w, inp, toks), "chunked prefill")
 
 
@@ -322,10 +331,12 @@ def test_router_bias_for_selection_only(T, path):
     w = custom(f"biassel{T}", T=T, skewed=True)
     inp = layer_inputs(w)
     layer = make_layer(w, path=path, bias_select_only=True)
-    got, y = gpu_run(w, inp, layer)
+    got, y, fwd = gpu_run(w, inp, layer, with_forward_tables=True)
     layer.close()
-    check_routing(got, oracle_routing(w, inp, bias_select_only=True))
-    toks = sample_tokens(w.T, 40)
+    ref = oracle_routing(w, inp, bias_select_only=True)
+    check_routing(got, ref)
+    check_routing(fwd, ref, "moe_forward")
+    toks = np.arange(w.T)
     check_y(y_host(y)[toks], oracle_y(w, inp, toks, bias_select_only=True), f"bias for selection only, T={T}")
     # the plain reading differs on these inputs: the bias also scales the weights there
     ref_plain = oracle_routing(w, inp)
@@ -346,10 +357,12 @@ def test_sigmoid_gated_shared_expert(T, path, x_dtype):
     d = device_inputs(w, inp)
     d["router_w"] = torch.cat([d["router_w"], torch.from_numpy(g)[None].to(d["router_w"].device)]).contiguous()
     layer = make_layer(w, path=path, shared_gate=True)
-    got, y = gpu_run(w, inp, layer, dev_in=d)
+    got, y, fwd = gpu_run(w, inp, layer, dev_in=d, with_forward_tables=True)
     layer.close()
-    check_routing(got, oracle_routing(w, inp))
-    toks = sample_tokens(w.T, 40)
+    ref = oracle_routing(w, inp)
+    check_routing(got, ref)
+    check_routing(fwd, ref, "moe_forward")
+    toks = np.arange(w.T)
     got_y = y_host(y)[toks]
     check_y(got_y, oracle_y(w, inp, toks, shared_gate_w=g), f"sigmoid-gated shared expert, T={T}")
     # the gate matters on these inputs: the ungated layer is outside the tolerance
@@ -362,7 +375,7 @@ def test_shared_gate_needs_a_shared_expert():
         moe.MoeLayer(512, 64, 256, 4, 16, has_shared=False, shared_gate=True)
 
 
-@pytest.mark.parametrize("T", [2, 3, 5, 8, 10])
+@pytest.mark.parametrize("T", [2, 3, 4, 5, 7, 8, 10])
 def test_fused_kernel_each_token_bound(T):
     # the fused kernel is instantiated for token bounds 1, 2, 4, 8 and 16; run
     # each bound at the decode shapes (d = 2048, 256 experts, inter 512,

@@ -1,9 +1,10 @@
 """The allocation-free decode entry point (moe_decode_noalloc) against the
 regular context-based one (moe_forward, small-T path), through the C ABI.
 
-Callers that cannot allocate device memory -- code recording work inside a
-CUDA stream capture, or running under a no-allocation policy -- use
-moe_decode_noalloc, whose scratch is a fixed device array inside the library.
+Callers that cannot allocate device memory -- a plugin whose host application
+owns every device buffer, or a serving loop that must not risk the device
+synchronisation an allocation may cause -- use moe_decode_noalloc, whose
+scratch is a fixed device array inside the library.
 Two calls in a row must both match moe_forward (the second one runs on the
 scratch contents the first one left behind).  This file is collected last so
 that a stop-at-first-failure run has already run every other test.
