@@ -194,14 +194,25 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------------ inputs
-def device_weights(w: mw.Workload, layer: int, dev, shared_gate=False):
+def device_weights(w: mw.Workload, layer: int, dev, shared_gate=False, q4=False):
     """Seeded device-side weights of one layer (torch CUDA generator).  With
     ``shared_gate`` the router gets a row E: the gate vector of a sigmoid-gated
-    shared expert, ~ N(0, 0.9^2 / d) like ``moe_workloads.draw_shared_gate``."""
+    shared expert, ~ N(0, 0.9^2 / d) like ``moe_workloads.draw_shared_gate``.
+    With ``q4`` the experts are 4-bit planes (MOE_W_Q4G64) drawn like
+    ``moe_workloads.draw_expert_q4``: uniform codes, per-group scale
+    0.02 / sqrt(21.25) (1 + 0.1 N(0, 1)) and bias -7.5 scale."""
     import torch
 
     g = torch.Generator(device=dev)
     g.manual_seed(w.seed * 1000 + layer)
+
+    def q4_planes(n_mats, rows, cols):
+        # every row: codes (cols / 8 u32), then scales and biases (cols / 64 bf16 each)
+        codes = torch.randint(-2 ** 31, 2 ** 31 - 1, (n_mats * rows, cols // 8), generator=g, device=dev,
+                              dtype=torch.int64).to(torch.int32)
+        s = (0.02 / 21.25 ** 0.5) * (1 + 0.1 * torch.randn(n_mats * rows, cols // 64, generator=g, device=dev))
+        params = torch.cat([s, -7.5 * s], dim=1).to(torch.bfloat16)
+        return torch.cat([codes.view(torch.uint8), params.view(torch.uint8)], dim=1).reshape(-1)
 
     def normal(*shape):
         out = torch.empty(*shape, dtype=torch.bfloat16, device=dev)
@@ -219,6 +230,10 @@ def device_weights(w: mw.Workload, layer: int, dev, shared_gate=False):
     router_b = None
     if w.skewed:
         router_b = torch.tensor(mw.draw_router(w, layer)[1], device=dev)
+    if q4:
+        shared = (torch.cat([q4_planes(1, 2 * w.I_s, w.d), q4_planes(1, w.d, w.I_s)]) if w.I_s else None)
+        return dict(router_w=router_w.contiguous(), router_b=router_b, gate_up=q4_planes(w.E, 2 * w.I, w.d),
+                    down=q4_planes(w.E, w.d, w.I), shared=shared)
     return dict(router_w=router_w.contiguous(), router_b=router_b, gate_up=normal(w.E, 2 * w.I, w.d),
                 down=normal(w.E, w.d, w.I), shared=normal(3 * w.I_s * w.d) if w.I_s else None)
 
@@ -233,16 +248,24 @@ def host_x(w: mw.Workload, layer: int):
 
 
 # ------------------------------------------------------------------ algorithmic bytes / flops
-def layer_costs(w: mw.Workload, idx: np.ndarray, shared_gate=False):
+def expert_matrix_bytes(rows: int, cols: int, q4: bool) -> int:
+    """Stored bytes of one expert weight matrix: bf16, or 4-bit codes (half a
+    byte per weight) plus a bf16 scale and bias per 64 weights."""
+    return rows * cols // 2 + rows * (cols // 64) * 4 if q4 else rows * cols * 2
+
+
+def layer_costs(w: mw.Workload, idx: np.ndarray, shared_gate=False, q4=False):
     """Bytes and flops a layer must move/compute, from its actual routing
-    (with ``shared_gate``, the router's extra gate row as well)."""
+    (with ``shared_gate``, the router's extra gate row as well; with ``q4``,
+    4-bit expert weights)."""
     distinct = len(np.unique(idx)) + (1 if w.I_s else 0)
-    expert_bytes = 3 * w.d * w.I * 2
+    gate_up_w = expert_matrix_bytes(2 * w.I, w.d, q4)
+    expert_bytes = gate_up_w + expert_matrix_bytes(w.d, w.I, q4)
     xb = 2 if w.x_dtype == "bf16" else 4
     rows = w.T * (w.k + (1 if w.I_s else 0))
     return dict(
         distinct=distinct,
-        gate_up_bytes=distinct * 2 * w.I * w.d * 2 + w.T * w.d * xb,
+        gate_up_bytes=distinct * gate_up_w + w.T * w.d * xb,
         layer_bytes=distinct * expert_bytes + (w.E + int(shared_gate)) * w.d * 4 + 2 * w.T * w.d * xb,
         gate_up_flops=2.0 * rows * w.d * 2 * w.I,
         layer_flops=2.0 * rows * 3 * w.d * w.I,
@@ -270,18 +293,33 @@ def oracle_sample(w: mw.Workload, budget_s: float, host_inputs):
     done, t0 = 0, time.perf_counter()
     while True:
         for inp in host_inputs:
-            oracle.moe_layer(inp["x"], inp["router_w"], inp["router_b"], inp["gate_up"], inp["down"], inp["shared"],
+            gu, dn, sh, f64 = inp["gate_up"], inp["down"], inp["shared"], False
+            if inp.get("q4_gate_up") is not None:  # 4-bit experts: the oracle expands them (step of its definition)
+                gu, dn, f64 = oracle.dequant_affine4(*inp["q4_gate_up"]), oracle.dequant_affine4(*inp["q4_down"]), True
+                if inp["q4_shared"] is not None:
+                    sh = tuple(oracle.dequant_affine4(*m)[0] for m in inp["q4_shared"])
+            oracle.moe_layer(inp["x"], inp["router_w"], inp["router_b"], gu, dn, sh,
                              w.k, x_bf16=w.x_dtype == "bf16", tokens=inp["tokens"], expert_ids=inp["expert_ids"],
-                             shared_gate_w=inp.get("shared_gate_w"))
+                             shared_gate_w=inp.get("shared_gate_w"), weights_f64=f64)
             done += len(inp["tokens"])
         el = time.perf_counter() - t0
         if el >= budget_s:
             return done / el, done, el, threads
 
 
-def host_layer_for_oracle(w, layer, dev_w, x_host, n_tokens=8, seed=0):
+def unpack_q4_planes(buf: np.ndarray, n: int, rows: int, cols: int):
+    """The MOE_W_Q4G64 rows of n stacked [rows, cols] matrices in a byte buffer
+    -> (words [n, rows, cols / 8] u32, scales, biases [n, rows, cols / 64] bf16 bits)."""
+    r = buf[:n * rows * cols // 16 * 9].reshape(n, rows, cols // 16 * 9)
+    words = np.ascontiguousarray(r[..., :cols // 2]).view(np.uint32)
+    params = np.ascontiguousarray(r[..., cols // 2:]).view(np.uint16)
+    return words, params[..., :cols // 64], params[..., cols // 64:]
+
+
+def host_layer_for_oracle(w, layer, dev_w, x_host, n_tokens=8, seed=0, q4=False):
     """Host copies of what the oracle needs for a sample of one layer's tokens:
-    x, the router, the experts the oracle routes those tokens to, the shared expert."""
+    x, the router, the experts the oracle routes those tokens to, the shared expert
+    (with ``q4``: their 4-bit planes, which the timed oracle expands itself)."""
     import torch
 
     import oracle
@@ -297,6 +335,17 @@ def host_layer_for_oracle(w, layer, dev_w, x_host, n_tokens=8, seed=0):
     toks = np.sort(rng.choice(w.T, min(w.T, n_tokens), replace=False))
     logits = oracle.router_logits(oracle.as_f64(x, w.x_dtype == "bf16")[toks], wr.astype(np.float64), rb)
     used = np.unique(oracle.route(logits, w.k)[0])
+    if q4:
+        gu = unpack_q4_planes(dev_w["gate_up"].cpu().numpy(), w.E, 2 * w.I, w.d)
+        dn = unpack_q4_planes(dev_w["down"].cpu().numpy(), w.E, w.d, w.I)
+        sh = None
+        if dev_w["shared"] is not None:
+            b = dev_w["shared"].cpu().numpy()
+            n_gu = 2 * w.I_s * (w.d // 16 * 9)
+            sh = (unpack_q4_planes(b[:n_gu], 1, 2 * w.I_s, w.d), unpack_q4_planes(b[n_gu:], 1, w.d, w.I_s))
+        return dict(x=x, router_w=wr, router_b=rb, q4_gate_up=tuple(a[used] for a in gu),
+                    q4_down=tuple(a[used] for a in dn), q4_shared=sh, gate_up=None, down=None, shared=None,
+                    expert_ids=used, tokens=toks, shared_gate_w=gate)
     return dict(x=x, router_w=wr, router_b=rb, gate_up=bits(dev_w["gate_up"][torch.from_numpy(used).to(
         dev_w["gate_up"].device)]), down=bits(dev_w["down"][torch.from_numpy(used).to(dev_w["down"].device)]),
         shared=None if dev_w["shared"] is None else bits(dev_w["shared"]), expert_ids=used, tokens=toks,
@@ -344,7 +393,8 @@ def run_ours(args, rank, world, dev, workload=None, cpu_seconds=None, chunk=None
     torch.cuda.set_device(dev)
     stream = torch.cuda.Stream(device=dev)
 
-    weights = [device_weights(w, L, dev, args.shared_gate) for L in range(layers)]
+    q4 = args.weights == "q4"
+    weights = [device_weights(w, L, dev, args.shared_gate, q4) for L in range(layers)]
     # one pinned host block and one device block for all layers' tokens, so an
     # end-to-end step moves its inputs and results in one copy each way
     xh_all = torch.stack([host_x(w, replica_layer(L, rank)) for L in range(layers)]).pin_memory()
@@ -354,7 +404,8 @@ def run_ours(args, rank, world, dev, workload=None, cpu_seconds=None, chunk=None
     xh, xd, yd, yh = list(xh_all), list(xd_all), list(yd_all), list(yh_all)
     max_tokens = chunk if chunk else w.T
     ctx = moe.MoeLayer(w.d, w.E, w.I, w.k, max_tokens, x_dtype=moe.MOE_F32 if w.x_dtype == "f32" else moe.MOE_BF16,
-                       has_router_bias=w.skewed, has_shared=w.I_s > 0, shared_gate=args.shared_gate)
+                       has_router_bias=w.skewed, has_shared=w.I_s > 0, shared_gate=args.shared_gate,
+                       weight_format=moe.MOE_W_Q4G64 if q4 else moe.MOE_W_BF16)
     if chunk:  # chunked prefill: workspace for `chunk` tokens, the layer over all T in slices
         moe.moe_set_chunk_tokens(ctx.ctx, chunk)
     path = moe.MOE_PATH_AUTO if args.path == "auto" else (moe.MOE_PATH_GEMV if args.path == "gemv"
@@ -366,7 +417,8 @@ def run_ours(args, rank, world, dev, workload=None, cpu_seconds=None, chunk=None
     whole_layer = eff_path == moe.MOE_PATH_GEMV  # the dominant kernel is the whole layer
     # the configuration a traffic record must have been taken on (per-launch traffic
     # does not depend on the number of stacked layers)
-    traffic_key = w.name + ("+shared_gate" if args.shared_gate else "") + (f"+chunk{chunk}" if chunk else "")
+    traffic_key = (w.name + ("+shared_gate" if args.shared_gate else "") + (f"+chunk{chunk}" if chunk else "")
+                   + ("+q4" if q4 else ""))
     if layers > 1:
         # stacked layers with fixed weights: a layer's blocks may start on its
         # weights while the previous layer's kernel finishes (moe_set_overlap)
@@ -387,7 +439,7 @@ def run_ours(args, rank, world, dev, workload=None, cpu_seconds=None, chunk=None
                 q = weights[(L + 1) % layers]
                 moe.moe_set_prefetch(ctx.ctx, q["router_w"], q["shared"])
             moe.moe_forward(ctx.ctx, xd[L], p["router_w"], p["router_b"], p["gate_up"], p["down"], p["shared"], w.k,
-                            yd[L], stream)
+                            yd[L], stream, packed_weights=q4)
         if e2e:
             yh_all.copy_(yd_all, non_blocking=True)
         if ev_pair is not None and whole_layer:
@@ -401,7 +453,7 @@ def run_ours(args, rank, world, dev, workload=None, cpu_seconds=None, chunk=None
             step_t = chunk or w.T  # moe_route keeps the T <= max_tokens limit: route slice by slice
             idx = [ctx.route(xd[L][t0:t0 + step_t], p["router_w"], p["router_b"], stream=stream)["idx"].cpu().numpy()
                    for t0 in range(0, w.T, step_t)]
-            costs.append(layer_costs(w, np.concatenate(idx), args.shared_gate))
+            costs.append(layer_costs(w, np.concatenate(idx), args.shared_gate, q4))
         for _ in range(max(args.warmup, 0)):
             step()
     stream.synchronize()
@@ -527,15 +579,16 @@ def run_ours(args, rank, world, dev, workload=None, cpu_seconds=None, chunk=None
     if rank == 0:
         cpu = None
         if not args.no_cpu_baseline and world == 1:
-            hosts = [host_layer_for_oracle(w, L, weights[L], xh[L]) for L in range(layers)]
+            hosts = [host_layer_for_oracle(w, L, weights[L], xh[L], q4=q4) for L in range(layers)]
             v, n, el, thr = oracle_sample(w, cpu_seconds, hosts)
             cpu = dict(value=round(v, 3), unit=UNIT, cores=thr, kind="oracle",
                        sample=f"{n} token-layers (8 random tokens per layer, all {layers} layers, repeated) "
                               f"in {el:.1f} s; fp64 numpy, BLAS threads = {thr}")
         out = dict(metric=METRIC, value=round(value, 1), unit=UNIT, n_gpus=world, steps=args.steps,
                    warmup=args.warmup, ms_per_step=round(ms_step, 5), higher_is_better=True, scaling="weak",
-                   vs_baseline=None, dtype="bf16", data="synthetic",
+                   vs_baseline=None, dtype="q4" if q4 else "bf16", data="synthetic",
                    config=dict(workload=w.name, tokens_per_layer=w.T, layers_per_step=layers, d=w.d, experts=w.E,
+                               weights="q4g64 (4-bit codes, bf16 scale + bias per 64)" if q4 else "bf16",
                                inter=w.I, shared_inter=w.I_s, top_k=w.k,
                                path="gemv" if eff_path == moe.MOE_PATH_GEMV else "grouped_gemm",
                                l2=(f"inputs larger than L2 (distinct weights per layer, "
@@ -614,6 +667,8 @@ def main():
                     help="stacked layers per step (default: the workload's own; fewer only for small profiling runs)")
     ap.add_argument("--shared-gate", action="store_true",
                     help="the sigmoid-gated shared-expert variant (a gate row appended to the router)")
+    ap.add_argument("--weights", default="bf16", choices=["bf16", "q4"],
+                    help="expert weight format: bf16, or 4-bit group-affine (MOE_W_Q4G64)")
     ap.add_argument("--no-prefill", action="store_true",
                     help="decode only: skip the nested prefill_balanced / prefill_skewed measurements")
     ap.add_argument("--prefill-cpu-seconds", type=float, default=6.0,

@@ -17,6 +17,7 @@ from ._build import LIB, build  # noqa: F401
 MOE_OK, MOE_ERR_ARG, MOE_ERR_ALIGN, MOE_ERR_UNSUPPORTED, MOE_ERR_CUDA, MOE_ERR_TIMEOUT, MOE_ERR_BOUNDS, \
     MOE_ERR_NOMEM = range(8)
 MOE_F32, MOE_BF16 = 0, 1
+MOE_W_BF16, MOE_W_Q4G64 = 0, 1
 MOE_PATH_AUTO, MOE_PATH_GEMV, MOE_PATH_GEMM = 0, 1, 2
 MOE_ROUTER_AUTO, MOE_ROUTER_SIMT, MOE_ROUTER_TENSOR = 0, 1, 2
 (MOE_K_ROUTER, MOE_K_SELECT, MOE_K_GROUP, MOE_K_GEMV_GATE_UP, MOE_K_GEMV_DOWN, MOE_K_GEMM_GATE_UP, MOE_K_GEMM_DOWN,
@@ -34,7 +35,7 @@ class MoeError(RuntimeError):
 class moe_config(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int) for n in ("d", "n_experts", "inter", "shared_inter", "top_k", "max_tokens",
                                             "x_dtype", "has_router_bias", "has_shared", "bias_select_only",
-                                            "shared_gate")]
+                                            "shared_gate", "weight_format")]
 
 
 _lib = None
@@ -122,9 +123,10 @@ def moe_strerror(code: int) -> str:
 
 
 def moe_init(d, n_experts, inter, shared_inter, top_k, max_tokens, x_dtype=MOE_BF16, has_router_bias=False,
-             has_shared=True, bias_select_only=False, shared_gate=False) -> ctypes.c_void_p:
+             has_shared=True, bias_select_only=False, shared_gate=False,
+             weight_format=MOE_W_BF16) -> ctypes.c_void_p:
     cfg = moe_config(d, n_experts, inter, shared_inter, top_k, max_tokens, x_dtype, int(has_router_bias),
-                     int(has_shared), int(bias_select_only), int(shared_gate))
+                     int(has_shared), int(bias_select_only), int(shared_gate), int(weight_format))
     h = ctypes.c_void_p()
     _check(lib().moe_init(ctypes.byref(cfg), ctypes.byref(h)), "moe_init")
     return h
@@ -199,12 +201,15 @@ def moe_route(ctx, x, router_w, router_b, top_k, idx=None, w=None, counts=None, 
 
 
 def moe_forward(ctx, x, router_w, router_b, experts_gate_up, experts_down, shared_w, top_k, y,
-                stream=None) -> None:
+                stream=None, packed_weights=False) -> None:
+    """``packed_weights``: the expert tensors are 4-bit planes (MOE_W_Q4G64, see
+    moe.h), passed as raw byte buffers of any dtype."""
     import torch
 
+    wdt = None if packed_weights else torch.bfloat16
     for name, t, dt in (("x", x, None), ("router_w", router_w, torch.float32), ("router_b", router_b, torch.float32),
-                        ("experts_gate_up", experts_gate_up, torch.bfloat16),
-                        ("experts_down", experts_down, torch.bfloat16), ("shared_w", shared_w, torch.bfloat16),
+                        ("experts_gate_up", experts_gate_up, wdt),
+                        ("experts_down", experts_down, wdt), ("shared_w", shared_w, wdt),
                         ("y", y, x.dtype)):
         _need_cuda(t, name, dt)
     _check(lib().moe_forward(ctx, _ptr(x), x.shape[0], _ptr(router_w), _ptr(router_b), _ptr(experts_gate_up),
@@ -257,22 +262,27 @@ class MoeLayer:
     """Owns one context; ``forward`` / ``route`` call the C ABI on torch tensors."""
 
     def __init__(self, d, n_experts, inter, top_k, max_tokens, *, shared_inter=None, x_dtype=MOE_BF16,
-                 has_router_bias=False, has_shared=True, bias_select_only=False, shared_gate=False):
+                 has_router_bias=False, has_shared=True, bias_select_only=False, shared_gate=False,
+                 weight_format=MOE_W_BF16):
         """``shared_gate``: sigmoid-gated shared expert; router_w then holds n_experts + 1
-        rows, the last being the gate vector."""
+        rows, the last being the gate vector.  ``weight_format``: MOE_W_BF16, or
+        MOE_W_Q4G64 for 4-bit experts (planes as in moe.h; see ``pack_q4``)."""
         self.top_k = top_k
         self.d = d
         self.n_experts = n_experts
         self.x_dtype = x_dtype
+        self.weight_format = weight_format
         self.ctx = moe_init(d, n_experts, inter, inter if shared_inter is None else shared_inter, top_k,
-                            max_tokens, x_dtype, has_router_bias, has_shared, bias_select_only, shared_gate)
+                            max_tokens, x_dtype, has_router_bias, has_shared, bias_select_only, shared_gate,
+                            weight_format)
 
     def forward(self, x, router_w, router_b, gate_up, down, shared_w, y=None, top_k=None, stream=None):
         import torch
 
         if y is None:
             y = torch.empty_like(x)
-        moe_forward(self.ctx, x, router_w, router_b, gate_up, down, shared_w, top_k or self.top_k, y, stream)
+        moe_forward(self.ctx, x, router_w, router_b, gate_up, down, shared_w, top_k or self.top_k, y, stream,
+                    packed_weights=self.weight_format == MOE_W_Q4G64)
         return y
 
     def route(self, x, router_w, router_b, top_k=None, stream=None):

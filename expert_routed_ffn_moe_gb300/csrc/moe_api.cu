@@ -83,6 +83,23 @@ int make_map(moe_ctx* ctx, CUtensorMap* m, const void* ptr, uint64_t inner, uint
   return r == CUDA_SUCCESS ? MOE_OK : MOE_ERR_CUDA;
 }
 
+// A 2-D map over 4-bit weight rows (9 K / 16 bytes each, `rows` of them): as
+// uint32 words (codes; box 8 words) or as bf16 (scales / biases; box 8 values),
+// `box_rows` rows per box, no swizzle.
+int make_q4_map(moe_ctx* ctx, CUtensorMap* m, const void* ptr, uint64_t K, uint64_t rows, uint32_t box_rows,
+                bool codes) {
+  const uint64_t row_bytes = K / 16 * 9;
+  const cuuint64_t dims[2] = {codes ? row_bytes / 4 : row_bytes / 2, rows};
+  const cuuint64_t strides[1] = {row_bytes};
+  const cuuint32_t box[2] = {8, box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r = ctx->encode(m, codes ? CU_TENSOR_MAP_DATA_TYPE_UINT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                                 const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                                 CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? MOE_OK : MOE_ERR_CUDA;
+}
+
 int check_route_args(moe_ctx* ctx, const void* x, int T, const float* wr, const float* rb, int top_k) {
   if (!ctx || T < 0) return MOE_ERR_ARG;
   if (T == 0) return MOE_OK;
@@ -106,6 +123,7 @@ Shapes shapes(const moe_ctx* ctx, int T, int top_k) {
   s.x_bf16 = c.x_dtype == MOE_BF16;
   s.bias_sel = c.has_router_bias && c.bias_select_only;
   s.shared_gate = c.has_shared && c.shared_gate;
+  s.q4 = c.weight_format == MOE_W_Q4G64;
   return s;
 }
 
@@ -208,6 +226,8 @@ int moe_init(const moe_config* cfg, moe_ctx** out) {
   if (c.bias_select_only != 0 && c.bias_select_only != 1) return MOE_ERR_ARG;
   if (c.shared_gate != 0 && c.shared_gate != 1) return MOE_ERR_ARG;
   if (c.shared_gate && !c.has_shared) return MOE_ERR_ARG;
+  if (c.weight_format != MOE_W_BF16 && c.weight_format != MOE_W_Q4G64) return MOE_ERR_ARG;
+  if (c.weight_format == MOE_W_Q4G64 && c.inter % 256 != 0) return MOE_ERR_UNSUPPORTED;
   if ((long long)c.max_tokens * (c.top_k + 1) >= (1LL << 31) / 2) return MOE_ERR_UNSUPPORTED;
 
   int dev = 0;
@@ -228,7 +248,7 @@ int moe_init(const moe_config* cfg, moe_ctx** out) {
   ctx->device = dev;
   ctx->num_sms = prop.multiProcessorCount;
   ctx->spin_ns = kDefaultSpinNs;
-  ctx->gemv_max_t = gemv_limit(ctx->cfg);
+  ctx->gemv_max_t = c.weight_format == MOE_W_BF16 ? gemv_limit(ctx->cfg) : 0;  // the modular GEMV kernels read bf16
   for (int t = 1; t <= 16 && t <= c.max_tokens; ++t) {
     Shapes s1{};
     s1.T = t;
@@ -239,6 +259,7 @@ int moe_init(const moe_config* cfg, moe_ctx** out) {
     s1.has_shared = c.has_shared;
     s1.x_bf16 = c.x_dtype == MOE_BF16;
     s1.shared_gate = c.has_shared && c.shared_gate;
+    s1.q4 = c.weight_format == MOE_W_Q4G64;
     if (decode_supported(s1, kDecodeSmemLimit) && decode_blocks_per_sm(s1, kDecodeSmemLimit) >= 1) ctx->decode_max_t = t;
   }
 
@@ -506,21 +527,39 @@ static int forward_one(moe_ctx* ctx, const void* x, int T, const float* router_w
   }
 
   // grouped-GEMM path
+  if (s.q4 && !gemm_q4_supported(s.d, s.I)) return MOE_ERR_UNSUPPORTED;
   const bool tensor = use_tensor_router(ctx, s);
   GemmMaps maps;
   memset(&maps, 0, sizeof(maps));
   const uint64_t rows = (uint64_t)s.T * s.k + (s.has_shared ? s.T : 0);
   if (s.x_bf16 && (rc = make_map(ctx, &maps.x_tile, x, s.d, s.T, 64, 128)) != MOE_OK) return rc;
   if ((rc = make_map(ctx, &maps.x_perm, ctx->sc.x_perm, s.d, rows, 64, 128)) != MOE_OK) return rc;
-  if ((rc = make_map(ctx, &maps.gate_up, gu, s.d, (uint64_t)s.E * 2 * s.I, 64, 128)) != MOE_OK) return rc;
   if ((rc = make_map(ctx, &maps.h, ctx->sc.h, s.I, rows, 64, 128)) != MOE_OK) return rc;
-  if ((rc = make_map(ctx, &maps.down, dn, s.I, (uint64_t)s.E * s.d, 64, 256)) != MOE_OK) return rc;
   if ((rc = make_map(ctx, &maps.wr_split, ctx->sc.wr_split, s.d, 3 * s.E, 64, 256)) != MOE_OK) return rc;
-  // without a shared expert these maps are never read; point them at routed weights
-  const uint16_t* sgu = sw ? sw : gu;
-  const uint16_t* sdn = sw ? sw + (size_t)2 * s.I * s.d : dn;
-  if ((rc = make_map(ctx, &maps.shared_gu, sgu, s.d, 2 * s.I, 64, 128)) != MOE_OK) return rc;
-  if ((rc = make_map(ctx, &maps.shared_down, sdn, s.I, s.d, 64, 256)) != MOE_OK) return rc;
+  if (s.q4) {
+    // 4-bit rows: the routed experts, and the shared expert's gate_up rows followed by its down rows
+    const uint8_t* gq = static_cast<const uint8_t*>(experts_gate_up);
+    const uint8_t* dq = static_cast<const uint8_t*>(experts_down);
+    const uint8_t* sgq = sw ? reinterpret_cast<const uint8_t*>(sw) : gq;
+    const uint8_t* sdq = sw ? sgq + (size_t)2 * s.I * (s.d / 16 * 9) : dq;
+    const uint64_t egu = (uint64_t)s.E * 2 * s.I, edn = (uint64_t)s.E * s.d;
+    if ((rc = make_q4_map(ctx, &maps.gu_codes, gq, s.d, egu, 128, true)) != MOE_OK) return rc;
+    if ((rc = make_q4_map(ctx, &maps.gu_params, gq, s.d, egu, 128, false)) != MOE_OK) return rc;
+    if ((rc = make_q4_map(ctx, &maps.dn_codes, dq, s.I, edn, 256, true)) != MOE_OK) return rc;
+    if ((rc = make_q4_map(ctx, &maps.dn_params, dq, s.I, edn, 256, false)) != MOE_OK) return rc;
+    if ((rc = make_q4_map(ctx, &maps.sgu_codes, sgq, s.d, 2 * s.I, 128, true)) != MOE_OK) return rc;
+    if ((rc = make_q4_map(ctx, &maps.sgu_params, sgq, s.d, 2 * s.I, 128, false)) != MOE_OK) return rc;
+    if ((rc = make_q4_map(ctx, &maps.sdn_codes, sdq, s.I, s.d, 256, true)) != MOE_OK) return rc;
+    if ((rc = make_q4_map(ctx, &maps.sdn_params, sdq, s.I, s.d, 256, false)) != MOE_OK) return rc;
+  } else {
+    if ((rc = make_map(ctx, &maps.gate_up, gu, s.d, (uint64_t)s.E * 2 * s.I, 64, 128)) != MOE_OK) return rc;
+    if ((rc = make_map(ctx, &maps.down, dn, s.I, (uint64_t)s.E * s.d, 64, 256)) != MOE_OK) return rc;
+    // without a shared expert these maps are never read; point them at routed weights
+    const uint16_t* sgu = sw ? sw : gu;
+    const uint16_t* sdn = sw ? sw + (size_t)2 * s.I * s.d : dn;
+    if ((rc = make_map(ctx, &maps.shared_gu, sgu, s.d, 2 * s.I, 64, 128)) != MOE_OK) return rc;
+    if ((rc = make_map(ctx, &maps.shared_down, sdn, s.I, s.d, 64, 256)) != MOE_OK) return rc;
+  }
 
   // routing, grouping, and the token rows written in grouped order (x_perm)
   if ((rc = run_route(ctx, s, x, router_w, router_b, tensor, &maps, st, true)) != MOE_OK) return rc;

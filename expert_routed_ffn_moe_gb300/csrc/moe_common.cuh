@@ -161,6 +161,10 @@ MOE_DEV float warp_pick_weight(float lu, int k, int lane) {
   return __fdividef(ex, den);
 }
 
+// Order this thread's generic-proxy shared-memory writes before later
+// async-proxy accesses (TMA, tcgen05.mma) that a barrier hands them to.
+MOE_DEV void fence_proxy_async_shared_cta() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
 MOE_DEV uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }

@@ -15,12 +15,26 @@ const void* decode_kernel_maxt2(const Shapes& s);
 const void* decode_kernel_maxt4(const Shapes& s);
 const void* decode_kernel_maxt8(const Shapes& s);
 const void* decode_kernel_maxt16(const Shapes& s);
+// defined in moe_decode_q4_k<MAXT>.cu (4-bit weights)
+const void* decode_kernel_q4_maxt1(const Shapes& s);
+const void* decode_kernel_q4_maxt2(const Shapes& s);
+const void* decode_kernel_q4_maxt4(const Shapes& s);
+const void* decode_kernel_q4_maxt8(const Shapes& s);
+const void* decode_kernel_q4_maxt16(const Shapes& s);
 
 // The smallest instantiated token bound MAXT >= T: the per-token loops of
 // phases B and C are unrolled over MAXT, so a tight bound saves issue slots
 // (measured at d = 2048, I = 512: T = 4 took 101 us per layer with MAXT = 16,
 // 66 us with MAXT = 4).
 static const void* decode_kernel_for(const Shapes& s) {
+  if (s.q4) {
+    if (s.T <= 1) return decode_kernel_q4_maxt1(s);
+    if (s.T <= 2) return decode_kernel_q4_maxt2(s);
+    if (s.T <= 4) return decode_kernel_q4_maxt4(s);
+    if (s.T <= 8) return decode_kernel_q4_maxt8(s);
+    if (s.T <= 16) return decode_kernel_q4_maxt16(s);
+    return nullptr;
+  }
   if (s.T <= 1) return decode_kernel_maxt1(s);
   if (s.T <= 2) return decode_kernel_maxt2(s);
   if (s.T <= 4) return decode_kernel_maxt4(s);
@@ -59,9 +73,13 @@ static int decode_dyn_limit(const void* k) {
   return lim;
 }
 
-// The weight ring: slots hold one gate/up unit (2 d bf16) or the down rows of
-// top_k + 1 experts (a whole phase-C row at batch 1), whichever is larger; as
-// many slots as the shared memory left after x / h holds, up to kMaxSlots.
+// The weight ring: slots hold one gate/up unit (2 d bf16, or the two 4-bit
+// code rows and their parameters) or the down rows of top_k + 1 experts (a
+// whole phase-C row at batch 1), whichever is larger; as many slots as the
+// shared memory left after x / h holds, up to kRingSlots (bf16) or
+// kRingSlotsQ4 (4-bit items are 3.7 times smaller, so more of them must be in
+// flight to cover the same memory latency).
+constexpr int kRingSlotsQ4 = kMaxSlots;
 struct DecodeRing {
   int slots, slot_bytes, chunk;
 };
@@ -71,11 +89,16 @@ static DecodeRing decode_ring(const Shapes& s, int max_smem) {
   if (!k) return r;
   const int lim = decode_dyn_limit(k);
   const long long budget = (long long)(max_smem < lim ? max_smem : lim) - (long long)decode_big_bytes(s);
-  const int unit = 4 * s.d, drow = 2 * s.I * (s.k + 1);
-  r.slot_bytes = unit > drow ? unit : drow;
-  r.chunk = r.slot_bytes / (2 * s.I);
+  // bytes of one gate/up unit and of one expert's down row
+  const int unit = s.q4 ? s.d + s.d / 8 : 4 * s.d;
+  const int drow1 = s.q4 ? s.I / 2 + s.I / 16 : 2 * s.I;
+  const int drow = drow1 * (s.k + 1);
+  const int widest = unit > drow ? unit : drow;
+  r.slot_bytes = (widest + 15) / 16 * 16;
+  r.chunk = r.slot_bytes / drow1;
   const long long n = budget > 0 ? budget / r.slot_bytes : 0;
-  r.slots = (int)(n < kRingSlots ? n : kRingSlots);
+  const int cap = s.q4 ? kRingSlotsQ4 : kRingSlots;
+  r.slots = (int)(n < cap ? n : cap);
   return r;
 }
 
@@ -94,12 +117,13 @@ cudaError_t prepare_decode_kernels(int max_smem) {
   for (int T : {1, 2, 4, 8, 16})
     for (int d : {512, 1024, 2048})
       for (int I : {256, 512, 1024})
-        for (int xb = 0; xb < 2; ++xb) {
+        for (int xb = 0; xb < 4; ++xb) {
           Shapes s{};
           s.T = T;
           s.d = d;
           s.I = I;
-          s.x_bf16 = xb;
+          s.x_bf16 = xb & 1;
+          s.q4 = xb >> 1;
           const void* k = decode_kernel_for(s);
           if (!k) continue;
           const int lim = decode_dyn_limit(k);
@@ -142,6 +166,9 @@ cudaError_t launch_decode_fused(const Shapes& s, const void* x, const float* wr,
   a.sc = sc;
   a.ctl = ctl;
   a.bar = bar;
+  // 4-bit weights: the shared expert's down rows follow its 2I gate_up rows (9 d / 16 bytes each)
+  a.sh_down_q4 = (s.q4 && shared_w) ? reinterpret_cast<const uint8_t*>(shared_w) + (size_t)2 * s.I * (s.d / 16 * 9)
+                                     : nullptr;
   const void* k = decode_kernel_for(s);
   if (!k) return cudaErrorInvalidValue;
   void* params[] = {&a};

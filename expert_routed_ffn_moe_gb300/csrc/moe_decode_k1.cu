@@ -3,6 +3,6 @@
 
 namespace moe {
 
-const void* decode_kernel_maxt1(const Shapes& s) { return pick_shape<1>(s); }
+const void* decode_kernel_maxt1(const Shapes& s) { return pick_shape<1, false>(s); }
 
 }  // namespace moe

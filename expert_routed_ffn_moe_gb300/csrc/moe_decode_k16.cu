@@ -3,6 +3,6 @@
 
 namespace moe {
 
-const void* decode_kernel_maxt16(const Shapes& s) { return pick_shape<16>(s); }
+const void* decode_kernel_maxt16(const Shapes& s) { return pick_shape<16, false>(s); }
 
 }  // namespace moe

@@ -3,6 +3,6 @@
 
 namespace moe {
 
-const void* decode_kernel_maxt2(const Shapes& s) { return pick_shape<2>(s); }
+const void* decode_kernel_maxt2(const Shapes& s) { return pick_shape<2, false>(s); }
 
 }  // namespace moe

@@ -3,6 +3,6 @@
 
 namespace moe {
 
-const void* decode_kernel_maxt4(const Shapes& s) { return pick_shape<4>(s); }
+const void* decode_kernel_maxt4(const Shapes& s) { return pick_shape<4, false>(s); }
 
 }  // namespace moe

@@ -3,6 +3,6 @@
 
 namespace moe {
 
-const void* decode_kernel_maxt8(const Shapes& s) { return pick_shape<8>(s); }
+const void* decode_kernel_maxt8(const Shapes& s) { return pick_shape<8, false>(s); }
 
 }  // namespace moe

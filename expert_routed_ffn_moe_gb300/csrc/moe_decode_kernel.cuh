@@ -60,7 +60,7 @@ constexpr int kWarps = 16;
 constexpr int kRowChunks = 4;                    // warps sharing one router row
 constexpr int kSlots = kWarps / kRowChunks;      // router rows per pass
 constexpr int kThreads = kWarps * 32;
-constexpr int kMaxSlots = 32;                    // TMA ring slots (array bound)
+constexpr int kMaxSlots = 48;                    // TMA ring slots (array bound)
 // Ring depth used: measured at batch 1 (d = 2048, 9 active experts), 14 slots
 // of 9 KB beat both 12 (too little in flight) and 16..22 (more bytes queued per
 // SM only spread the blocks' finishing times further apart).
@@ -139,6 +139,10 @@ struct DecodeArgs {
   int ring_slots;     // S: slots of the weight ring in shared memory (2..kMaxSlots)
   int slot_bytes;     // bytes per slot: max(gate + up row, chunk_experts down rows)
   int chunk_experts;  // down-projection rows (one per active expert) per slot
+  // 4-bit group-affine weights (s.q4): every row of K weights is 9 K / 16
+  // bytes, its code words (8 codes per word, lowest nibble first), then its
+  // K / 64 bf16 scales, then its K / 64 bf16 biases
+  const uint8_t* sh_down_q4;  // the shared expert's down rows (behind its gate_up rows)
 };
 
 // The 64-bit epoch counter of the fused decode kernel inside its control
@@ -166,7 +170,37 @@ MOE_DEV void issue_item(const DecodeArgs& A, int q, int slot, int n_sh, int nu, 
   const Shapes& s = A.s;
   uint8_t* dst = ring + (size_t)slot * A.slot_bytes;
   const uint64_t pol = policy_evict_first();
-  if (q < n_sh) {
+  if (s.q4) {
+    // 4-bit items: a gate/up unit is [gate row | up row], a phase-C chunk the
+    // rows r of its experts, back to back; each row carries its own scales and
+    // biases behind its codes, so one copy moves it
+    if (q < n_sh || q - n_sh < nu) {
+      const uint32_t row = (uint32_t)s.d / 16 * 9;
+      const uint8_t* W;
+      int i;
+      if (q < n_sh) {
+        i = b + q * G;
+        W = reinterpret_cast<const uint8_t*>(A.shared_w);
+      } else {
+        const int u = b + (q - n_sh) * G, a = u / s.I;
+        i = u - a * s.I;
+        W = reinterpret_cast<const uint8_t*>(A.gate_up) + (size_t)act_e[a] * 2 * s.I * row;
+      }
+      mbar_expect_tx(&full[slot], 2 * row);
+      bulk_g2s(dst, W + (size_t)i * row, row, &full[slot], pol);
+      bulk_g2s(dst + row, W + (size_t)(s.I + i) * row, row, &full[slot], pol);
+    } else {
+      const int m = q - n_sh - nu, j = m / nch, c = m - j * nch;
+      const int r = b + j * G, a0 = c * A.chunk_experts, na = min(A.chunk_experts, n_act - a0);
+      const uint32_t row = (uint32_t)s.I / 16 * 9;
+      mbar_expect_tx(&full[slot], (uint32_t)na * row);
+      for (int qa = 0; qa < na; ++qa) {
+        const int e = act_e[a0 + qa];
+        const uint8_t* Wd = (e < s.E) ? reinterpret_cast<const uint8_t*>(A.down) + (size_t)e * s.d * row : A.sh_down_q4;
+        bulk_g2s(dst + (size_t)qa * row, Wd + (size_t)r * row, row, &full[slot], pol);
+      }
+    }
+  } else if (q < n_sh) {
     const int i = b + q * G;
     const uint32_t row = (uint32_t)s.d * 2;
     mbar_expect_tx(&full[slot], 2 * row);
@@ -231,15 +265,91 @@ struct DecodeSmem {
   size_t total;
 };
 
+// With 4-bit weights the region also holds, behind x (or h), the sums of each
+// run of 8 consecutive values (one per 32-bit code word): d / 8 floats per
+// token (I / 8 per grouped h row).
 __host__ __device__ inline size_t decode_big_bytes(const Shapes& s) {
   const size_t pairs = (size_t)s.T * s.k + (s.has_shared ? s.T : 0);
-  const size_t a = (size_t)s.T * s.d * 4, b = pairs * s.I * 4;
+  size_t a = (size_t)s.T * s.d * 4, b = pairs * s.I * 4;
+  if (s.q4) {
+    a += a / 8;
+    b += b / 8;
+  }
   return a > b ? a : b;
+}
+
+// 1 + q / 16 for the 4-bit code q in bits [4 NIB, 4 NIB + 3] of w, built as an
+// fp32 bit pattern (q lands in mantissa bits 19..22): exact, one shift and
+// one bitwise operation.
+template <int NIB>
+MOE_DEV float q4_one_plus(uint32_t w) {
+  constexpr int sh = 19 - 4 * NIB;
+  const uint32_t v = sh >= 0 ? (w << sh) : (w >> (-sh));
+  return __uint_as_float((v & 0x00780000u) | 0x3F800000u);
+}
+// sum_i (1 + q_i / 16) a_i over the 8 codes of word w and a[0..7]
+MOE_DEV float q4_dot8(uint32_t w, const float4 a0, const float4 a1) {
+  float r = q4_one_plus<0>(w) * a0.x;
+  r = fmaf(q4_one_plus<1>(w), a0.y, r);
+  r = fmaf(q4_one_plus<2>(w), a0.z, r);
+  r = fmaf(q4_one_plus<3>(w), a0.w, r);
+  r = fmaf(q4_one_plus<4>(w), a1.x, r);
+  r = fmaf(q4_one_plus<5>(w), a1.y, r);
+  r = fmaf(q4_one_plus<6>(w), a1.z, r);
+  return fmaf(q4_one_plus<7>(w), a1.w, r);
+}
+// One word's share of a 4-bit row dot product: with sum_i (1 + q_i/16) a_i =
+// raw and sum_i a_i = as, sum_i (s q_i + b) a_i = 16 s raw + (b - 16 s) as.
+MOE_DEV float q4_word(float raw, float as, uint16_t s_bits, uint16_t b_bits, float acc) {
+  const float sc = __uint_as_float((uint32_t)s_bits << 16), bi = __uint_as_float((uint32_t)b_bits << 16);
+  return fmaf(16.f * sc, raw, fmaf(bi - 16.f * sc, as, acc));
+}
+// Gate and up dot products of one 4-bit unit (gate row, then up row, each
+// [codes | scales | biases]) against one token row: lane takes code words
+// lane + 32 c (NW per lane); x fp32 [d] and its 8-sums xs [d / 8].
+template <int NW>
+MOE_DEV void q4_unit_dot(const uint8_t* slot, int d, const float* x, const float* xs, int lane, float& g, float& u) {
+  const uint32_t* gc = reinterpret_cast<const uint32_t*>(slot);
+  const uint32_t* uc = reinterpret_cast<const uint32_t*>(slot + d / 16 * 9);
+  const uint16_t* gp = reinterpret_cast<const uint16_t*>(slot + d / 2);
+  const uint16_t* up = reinterpret_cast<const uint16_t*>(slot + d / 16 * 9 + d / 2);
+  const int ng = d / 64;
+  // two words per step, not fully unrolled: the fully unrolled dot of two
+  // phases made the kernel stall on instruction fetch
+#pragma unroll 2
+  for (int c = 0; c < NW; ++c) {
+    const int w = lane + 32 * c, grp = w >> 3;
+    const float4 a0 = reinterpret_cast<const float4*>(x)[2 * w], a1 = reinterpret_cast<const float4*>(x)[2 * w + 1];
+    const float as = xs[w];
+    g = q4_word(q4_dot8(gc[w], a0, a1), as, gp[grp], gp[ng + grp], g);
+    u = q4_word(q4_dot8(uc[w], a0, a1), as, up[grp], up[ng + grp], u);
+  }
+}
+// One 4-bit down row (I codes, NW words per lane) against one h row and its 8-sums.
+template <int NW>
+MOE_DEV float q4_row_dot(const uint32_t* codes, const uint16_t* params, int I, const float* h, const float* hs,
+                         int lane) {
+  const int ng = I / 64;
+  float acc = 0.f;
+#pragma unroll
+  for (int c = 0; c < NW; ++c) {
+    const int w = lane + 32 * c, grp = w >> 3;
+    const float4 a0 = reinterpret_cast<const float4*>(h)[2 * w], a1 = reinterpret_cast<const float4*>(h)[2 * w + 1];
+    acc = q4_word(q4_dot8(codes[w], a0, a1), hs[w], params[grp], params[ng + grp], acc);
+  }
+  return acc;
+}
+// The 8-sums of n consecutive runs of 8 floats (block-wide).
+MOE_DEV void sums_of_8(const float* v, float* out, int n, int tid, int nthreads) {
+  for (int i = tid; i < n; i += nthreads) {
+    const float4 a = reinterpret_cast<const float4*>(v)[2 * i], b = reinterpret_cast<const float4*>(v)[2 * i + 1];
+    out[i] = ((a.x + a.y) + (a.z + a.w)) + ((b.x + b.y) + (b.z + b.w));
+  }
 }
 
 // MAXT: compile-time bound on T (1, 2, 4, 8 or 16): the per-token loops unroll over it, and the
 // batch-1 kernel keeps one accumulator per lane.
-template <int NCH, int NCI, bool XBF16, int MAXT>
+template <int NCH, int NCI, bool XBF16, int MAXT, bool Q4>
 __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const DecodeArgs A) {
   extern __shared__ __align__(16) uint8_t dsm[];
   const Shapes& s = A.s;
@@ -335,6 +445,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const DecodeA
       for (int i = tid; i < nx / 2; i += kThreads) reinterpret_cast<float2*>(big)[i] = __ldg(xf + i);
     }
     __syncthreads();
+    if (Q4) {  // the 8-sums of x for the 4-bit dot products (behind x)
+      sums_of_8(big, big + nx, nx / 8, tid, kThreads);
+      __syncthreads();
+    }
     int n_e0 = 0;
     for (int e0 = b; e0 < s.E; e0 += kSlots * G) ++n_e0;
     for (int rep = 0; rep < n_e0; ++rep) {
@@ -391,10 +505,15 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const DecodeA
       const uint2* grow = reinterpret_cast<const uint2*>(ring + (size_t)slot * A.slot_bytes) + lane;
       const uint2* urow = grow + s.d / 4;
       for (int t = 0; t < s.T; ++t) {
-        const float4* xr = reinterpret_cast<const float4*>(big + (size_t)t * s.d) + lane;
         float g = 0.f, up = 0.f;
+        if (Q4) {
+          q4_unit_dot<NCH>(ring + (size_t)slot * A.slot_bytes, s.d, big + (size_t)t * s.d,
+                           big + (size_t)s.T * s.d + (size_t)t * (s.d / 8), lane, g, up);
+        } else {
+          const float4* xr = reinterpret_cast<const float4*>(big + (size_t)t * s.d) + lane;
 #pragma unroll
-        for (int c = 0; c < 2 * NCH; ++c) dot4x2(grow[32 * c], urow[32 * c], xr[32 * c], g, up);
+          for (int c = 0; c < 2 * NCH; ++c) dot4x2(grow[32 * c], urow[32 * c], xr[32 * c], g, up);
+        }
         g = warp_sum(g);
         up = warp_sum(up);
         if (lane < sc.dec_hreps) st_tagged(dh + (size_t)lane * hrep + ((size_t)tk + t) * s.I + i, silu(g) * up, ep_s);
@@ -591,9 +710,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const DecodeA
     const int nch = (n_act + A.chunk_experts - 1) / A.chunk_experts;
     n_items = n_sh + nu + nr * nch;
     // every slot is free (phase A consumed its items): fill all of them
-    if (warp == 0 && lane < S && n_sh + lane < n_items) {
-      fence_proxy_async_smem();  // after the phase-A reads of the slots, before the copies overwrite them
-      issue_item(A, n_sh + lane, (n_sh + lane) % S, n_sh, nu, nch, b, G, n_act, act_e, ring, full, slot_issued);
+    if (warp == 0) {
+      if (lane < S) fence_proxy_async_smem();  // after the phase-A reads of the slots, before the copies overwrite them
+      for (int q = n_sh + lane; q < n_sh + S && q < n_items; q += 32)
+        issue_item(A, q, q % S, n_sh, nu, nch, b, G, n_act, act_e, ring, full, slot_issued);
     }
     if (MAXT == 1 && b == 0 && sc.counts != nullptr && tid >= 32 && tid < 32 + s.E) {
       // batch 1: the layer's grouping tables, for moe_last_routing (one row per
@@ -628,10 +748,15 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const DecodeA
       while (mm) {
         const int t = __ffs(mm) - 1;
         mm &= mm - 1u;
-        const float4* xr = reinterpret_cast<const float4*>(big + (size_t)t * s.d) + lane;
         float g = 0.f, up = 0.f;
+        if (Q4) {
+          q4_unit_dot<NCH>(ring + (size_t)slot * A.slot_bytes, s.d, big + (size_t)t * s.d,
+                           big + (size_t)s.T * s.d + (size_t)t * (s.d / 8), lane, g, up);
+        } else {
+          const float4* xr = reinterpret_cast<const float4*>(big + (size_t)t * s.d) + lane;
 #pragma unroll
-        for (int c = 0; c < 2 * NCH; ++c) dot4x2(grow[32 * c], urow[32 * c], xr[32 * c], g, up);
+          for (int c = 0; c < 2 * NCH; ++c) dot4x2(grow[32 * c], urow[32 * c], xr[32 * c], g, up);
+        }
         g = warp_sum(g);
         up = warp_sum(up);
         if (lane < sc.dec_hreps) st_tagged(dh + (size_t)lane * hrep + (size_t)row * s.I + i, silu(g) * up, ep_s);
@@ -690,6 +815,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const DecodeA
       }
     }
     __syncthreads();
+    if (Q4) {  // the 8-sums of h for the 4-bit dot products (behind h)
+      sums_of_8(big, big + hrep, (int)(hrep / 8), tid, kThreads);
+      __syncthreads();
+    }
     ok = flag_s != 0;
   }
   if (ok) {
@@ -703,7 +832,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const DecodeA
     // pull them into L2 while this phase is bound by latency, not bandwidth
     // (the last warp: it has no output row when d < kWarps G)
     if (warp == kWarps - 1) {
-      const size_t rbytes = (size_t)(s.E + s.shared_gate) * s.d * 4, sbytes = (size_t)3 * s.I * s.d * 2;
+      // the shared expert's bytes: 3 I d bf16 weights, or 4-bit codes and parameters (27/16 I d bytes)
+      const size_t rbytes = (size_t)(s.E + s.shared_gate) * s.d * 4,
+                   sbytes = Q4 ? (size_t)27 * s.I * s.d / 16 : (size_t)3 * s.I * s.d * 2;
       const size_t rper = ((rbytes / G) + 4095) & ~size_t(4095), sper = ((sbytes / G) + 4095) & ~size_t(4095);
       if (A.next_wr)
         for (size_t off = rper * b + (size_t)lane * 4096; off < min(rbytes, rper * (b + 1)); off += 32 * 4096)
@@ -742,13 +873,21 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const DecodeA
               const int qa = qa0 + u;
               if (qa < na) {
                 const int a = a0 + qa;
-                const float4* hr = reinterpret_cast<const float4*>(big + (size_t)act_row[a] * s.I) + lane;
-                const uint2* wr = base + (size_t)qa * (s.I / 4);
                 float d0 = 0.f, d1 = 0.f;
+                if (Q4) {
+                  const uint8_t* rw = ring + (size_t)slot * A.slot_bytes + (size_t)qa * (s.I / 16 * 9);
+                  d0 = q4_row_dot<NCI>(reinterpret_cast<const uint32_t*>(rw),
+                                       reinterpret_cast<const uint16_t*>(rw + s.I / 2), s.I,
+                                       big + (size_t)act_row[a] * s.I, big + hrep + (size_t)act_row[a] * (s.I / 8),
+                                       lane);
+                } else {
+                  const float4* hr = reinterpret_cast<const float4*>(big + (size_t)act_row[a] * s.I) + lane;
+                  const uint2* wr = base + (size_t)qa * (s.I / 4);
 #pragma unroll
-                for (int cc = 0; cc < 2 * NCI; cc += 2) {
-                  d0 = dot4(wr[32 * cc], hr[32 * cc], d0);
-                  d1 = dot4(wr[32 * (cc + 1)], hr[32 * (cc + 1)], d1);
+                  for (int cc = 0; cc < 2 * NCI; cc += 2) {
+                    d0 = dot4(wr[32 * cc], hr[32 * cc], d0);
+                    d1 = dot4(wr[32 * (cc + 1)], hr[32 * (cc + 1)], d1);
+                  }
                 }
                 ps[u] = fmaf(act_w[a][0], d0 + d1, ps[u]);
               }
@@ -777,13 +916,20 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const DecodeA
                 const int a = pair_a[pu];
                 tt[u] = pair_t[pu];
                 ww[u] = act_w[a][tt[u]];
-                const uint2* wr = base + (size_t)(a - a0) * (s.I / 4);
-                const float4* hr = reinterpret_cast<const float4*>(big + (size_t)pu * s.I) + lane;
                 float d0 = 0.f, d1 = 0.f;
+                if (Q4) {
+                  const uint8_t* rw = ring + (size_t)slot * A.slot_bytes + (size_t)(a - a0) * (s.I / 16 * 9);
+                  d0 = q4_row_dot<NCI>(reinterpret_cast<const uint32_t*>(rw),
+                                       reinterpret_cast<const uint16_t*>(rw + s.I / 2), s.I, big + (size_t)pu * s.I,
+                                       big + hrep + (size_t)pu * (s.I / 8), lane);
+                } else {
+                  const uint2* wr = base + (size_t)(a - a0) * (s.I / 4);
+                  const float4* hr = reinterpret_cast<const float4*>(big + (size_t)pu * s.I) + lane;
 #pragma unroll
-                for (int cc = 0; cc < 2 * NCI; cc += 2) {
-                  d0 = dot4(wr[32 * cc], hr[32 * cc], d0);
-                  d1 = dot4(wr[32 * (cc + 1)], hr[32 * (cc + 1)], d1);
+                  for (int cc = 0; cc < 2 * NCI; cc += 2) {
+                    d0 = dot4(wr[32 * cc], hr[32 * cc], d0);
+                    d1 = dot4(wr[32 * (cc + 1)], hr[32 * (cc + 1)], d1);
+                  }
                 }
                 dd[u] = d0 + d1;
               }
@@ -852,26 +998,28 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const DecodeA
 }
 
 
-template <int NCH, int NCI, int MAXT>
+template <int NCH, int NCI, int MAXT, bool Q4>
 static const void* pick(bool xbf16) {
-  return xbf16 ? (const void*)decode_fused_kernel<NCH, NCI, true, MAXT>
-               : (const void*)decode_fused_kernel<NCH, NCI, false, MAXT>;
+  return xbf16 ? (const void*)decode_fused_kernel<NCH, NCI, true, MAXT, Q4>
+               : (const void*)decode_fused_kernel<NCH, NCI, false, MAXT, Q4>;
 }
 
-template <int MAXT>
+// The instantiation for a shape (d / 256 = NCH, I / 256 = NCI); Q4 selects
+// the 4-bit weight kernels (compiled in their own translation units).
+template <int MAXT, bool Q4>
 static const void* pick_shape(const Shapes& s) {
   const int nch = s.d / 256, nci = s.I / 256;
   if (nci == 2) {
-    if (nch == 2) return pick<2, 2, MAXT>(s.x_bf16);
-    if (nch == 4) return pick<4, 2, MAXT>(s.x_bf16);
-    if (nch == 8) return pick<8, 2, MAXT>(s.x_bf16);
+    if (nch == 2) return pick<2, 2, MAXT, Q4>(s.x_bf16);
+    if (nch == 4) return pick<4, 2, MAXT, Q4>(s.x_bf16);
+    if (nch == 8) return pick<8, 2, MAXT, Q4>(s.x_bf16);
   } else if (nci == 1) {
-    if (nch == 2) return pick<2, 1, MAXT>(s.x_bf16);
-    if (nch == 4) return pick<4, 1, MAXT>(s.x_bf16);
-    if (nch == 8) return pick<8, 1, MAXT>(s.x_bf16);
+    if (nch == 2) return pick<2, 1, MAXT, Q4>(s.x_bf16);
+    if (nch == 4) return pick<4, 1, MAXT, Q4>(s.x_bf16);
+    if (nch == 8) return pick<8, 1, MAXT, Q4>(s.x_bf16);
   } else if (nci == 4) {
-    if (nch == 4) return pick<4, 4, MAXT>(s.x_bf16);
-    if (nch == 8) return pick<8, 4, MAXT>(s.x_bf16);
+    if (nch == 4) return pick<4, 4, MAXT, Q4>(s.x_bf16);
+    if (nch == 8) return pick<8, 4, MAXT, Q4>(s.x_bf16);
   }
   return nullptr;
 }

@@ -28,6 +28,15 @@
 // Two accumulators let the epilogue of tile i overlap the main loop of tile
 // i + 1.  Every wait is bounded (MOE_ERR_TIMEOUT on expiry); on expiry the
 // kernel drains what it has in flight, frees TMEM and returns.
+//
+// 4-bit weights ("Optimizing on-device inference for Apple Silicon", section
+// "Dequantizing weights during matrix multiplication": the codes are expanded
+// one tile at a time inside the GEMM and never written out): the producer
+// loads each k block's raw codes (256 rows x 32 bytes) and, every 8 k blocks,
+// the rows' scales and biases of those 8 groups; 8 more warps expand the codes
+// to bf16, w = s q + b rounded once (bf16x2 fma), straight into the 128-byte
+// swizzled B tile the MMA reads, then release it to the MMA issuer.  3 stages
+// of (A 16 KB + B 32 KB + codes 8 KB) plus two 8 KB parameter buffers.
 #include "moe_internal.h"
 
 namespace moe {
@@ -44,10 +53,20 @@ constexpr int kBBytes = kBRows * kBK * 2;        // 32 KB
 constexpr int kThreads = 192;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kAccCols = 256;
+// 4-bit weights
+constexpr int kStagesQ4 = 3;
+constexpr int kRawBytes = kBRows * 32;           // one k block of codes: 256 rows x 8 words
+constexpr int kParGroups = 8;                    // groups (k blocks) per parameter load
+constexpr int kParBytes = kBRows * kParGroups * 2;  // scales (or biases) of 8 groups for 256 rows: 4 KB
+constexpr int kConvWarps = 8;                    // warps expanding codes (one B row per thread)
+constexpr int kThreadsQ4 = kThreads + kConvWarps * 32;
 
 struct __align__(8) Barriers {
   uint64_t full[kStages];
   uint64_t empty[kStages];
+  uint64_t conv[kStages];    // 4-bit: the stage's B tile has been expanded
+  uint64_t pfull[2];         // 4-bit: parameter buffer loaded
+  uint64_t pempty[2];        // 4-bit: parameter buffer consumed
   uint64_t tfull[2];
   uint64_t tempty[2];
   uint64_t mma_done;
@@ -56,6 +75,39 @@ struct __align__(8) Barriers {
 };
 
 constexpr size_t kSmemBytes = 1024 /*align slack*/ + (size_t)kStages * (kABytes + kBBytes) + sizeof(Barriers);
+constexpr size_t kSmemBytesQ4 = 1024 + (size_t)kStagesQ4 * (kABytes + kBBytes + kRawBytes) + 2 * 2 * kParBytes +
+                                sizeof(Barriers);
+
+// fma.rn.bf16x2: a * b + c per half, computed exactly and rounded once
+MOE_DEV uint32_t fma_bf16x2(uint32_t a, uint32_t b, uint32_t c) {
+  uint32_t d;
+  asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+MOE_DEV uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+  uint32_t d;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+  return d;
+}
+// The 8 weights of one code word (columns 8 c .. 8 c + 7 of the k block) as
+// bf16 s q + b.  A code q is made exact in bf16 as (128 + q) - 128: the bits
+// 0x4300 | q are the bf16 value 128 + q.  Nibbles i and i + 4 share a word
+// half-pair; prmt puts the columns back in order.
+MOE_DEV uint4 expand_q4_word(uint32_t w, uint32_t s2, uint32_t b2) {
+  constexpr uint32_t kMagic = 0x43004300u, kOne = 0x3F803F80u, kMinus128 = 0xC300C300u;
+  const uint32_t v0 = fma_bf16x2(fma_bf16x2((w & 0x000F000Fu) | kMagic, kOne, kMinus128), s2, b2);          // cols 0, 4
+  const uint32_t v1 = fma_bf16x2(fma_bf16x2(((w >> 4) & 0x000F000Fu) | kMagic, kOne, kMinus128), s2, b2);   // 1, 5
+  const uint32_t v2 = fma_bf16x2(fma_bf16x2(((w >> 8) & 0x000F000Fu) | kMagic, kOne, kMinus128), s2, b2);   // 2, 6
+  const uint32_t v3 = fma_bf16x2(fma_bf16x2(((w >> 12) & 0x000F000Fu) | kMagic, kOne, kMinus128), s2, b2);  // 3, 7
+  return make_uint4(prmt(v0, v1, 0x5410u), prmt(v2, v3, 0x5410u), prmt(v0, v1, 0x7632u), prmt(v2, v3, 0x7632u));
+}
+MOE_DEV void tma_load_2d_nohint(void* dst, const CUtensorMap* m, int c0, int c1, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+          smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(m)), "r"(c0), "r"(c1), "r"(smem_u32(bar))
+      : "memory");
+}
 
 struct Work {
   int e, row0, rows;   // expert (E = shared), first grouped row, valid rows
@@ -98,28 +150,38 @@ MOE_DEV void set_abort(Barriers* b) { *reinterpret_cast<volatile int*>(&b->abort
 
 }  // namespace
 
-template <int MODE>
-__global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_constant__ GemmMaps maps, Shapes s,
-                                                                   Scratch sc, DevCtl ctl, DevCtl drain) {
+// Q4: the B operand (weights) is expanded from 4-bit codes by the converter
+// warps 6 .. 6 + kConvWarps - 1 (gate/up and down modes only).
+template <int MODE, bool Q4>
+__global__ void __launch_bounds__(Q4 ? kThreadsQ4 : kThreads, 1)
+    grouped_gemm_kernel(const __grid_constant__ GemmMaps maps, Shapes s, Scratch sc, DevCtl ctl, DevCtl drain) {
+  constexpr int S = Q4 ? kStagesQ4 : kStages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* a_buf = base;
-  uint8_t* b_buf = base + kStages * kABytes;
-  Barriers* bar = reinterpret_cast<Barriers*>(b_buf + kStages * kBBytes);
+  uint8_t* b_buf = base + S * kABytes;
+  uint8_t* raw_buf = b_buf + S * kBBytes;                  // Q4: codes of each stage
+  uint8_t* par_buf = raw_buf + (Q4 ? S * kRawBytes : 0);   // Q4: [2 buffers][scales | biases]
+  Barriers* bar = reinterpret_cast<Barriers*>(par_buf + (Q4 ? 2 * 2 * kParBytes : 0));
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n_work = work_count<MODE>(s, sc);
   if ((int)blockIdx.x >= n_work) return;
-  const int KB = ((MODE == kDown) ? s.I : s.d) / kBK;
+  const int K = (MODE == kDown) ? s.I : s.d;   // reduction length
+  const int KB = K / kBK;
+  const int G = K / 64;                        // Q4: groups (of 64 columns) per weight row
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < kStages; ++i) {
+    for (int i = 0; i < S; ++i) {
       mbar_init(&bar->full[i], 1);
       mbar_init(&bar->empty[i], 1);
+      mbar_init(&bar->conv[i], kConvWarps * 32);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bar->tfull[i], 1);
       mbar_init(&bar->tempty[i], 128);
+      mbar_init(&bar->pfull[i], 1);
+      mbar_init(&bar->pempty[i], kConvWarps * 32);
     }
     mbar_init(&bar->mma_done, 1);
     bar->abort_flag = 0;
@@ -136,39 +198,81 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
     if (lane == 0) tma_prefetch_desc(MODE == kGateUp ? &maps.x_perm : (MODE == kDown ? &maps.h : &maps.x_tile));
     const uint64_t pol_w = policy_evict_normal();  // several m-tiles of one expert reuse its weights
     const uint64_t pol_a = policy_evict_last();
-    constexpr uint32_t tx = kABytes + kBBytes;
-    int it = 0;
+    constexpr uint32_t tx = kABytes + (Q4 ? kRawBytes : kBBytes);
+    int it = 0, pc = 0;
     bool ok = true;
     for (int w = blockIdx.x; w < n_work && ok; w += gridDim.x) {
       const Work wk = work_item<MODE>(s, sc, w);
       const CUtensorMap* mb;
+      const CUtensorMap* mp = nullptr;  // Q4: parameter view of the same rows
       int brow0, brow1 = 0;
       if (MODE == kGateUp) {
-        mb = (wk.e < s.E) ? &maps.gate_up : &maps.shared_gu;
+        mb = Q4 ? ((wk.e < s.E) ? &maps.gu_codes : &maps.sgu_codes) : ((wk.e < s.E) ? &maps.gate_up : &maps.shared_gu);
+        mp = (wk.e < s.E) ? &maps.gu_params : &maps.sgu_params;
         const int eb = (wk.e < s.E) ? wk.e * 2 * s.I : 0;
         brow0 = eb + wk.n0;
         brow1 = eb + s.I + wk.n0;
       } else if (MODE == kDown) {
-        mb = (wk.e < s.E) ? &maps.down : &maps.shared_down;
+        mb = Q4 ? ((wk.e < s.E) ? &maps.dn_codes : &maps.sdn_codes) : ((wk.e < s.E) ? &maps.down : &maps.shared_down);
+        mp = (wk.e < s.E) ? &maps.dn_params : &maps.sdn_params;
         brow0 = ((wk.e < s.E) ? wk.e * s.d : 0) + wk.n0;
       } else {
         mb = &maps.wr_split;
         brow0 = wk.part * s.E;
       }
       for (int kb = 0; kb < KB; ++kb, ++it) {
-        const int st = it % kStages;
+        const int st = it % S;
         if (lane == 0) {
-          bool good = mbar_wait(&bar->empty[st], ((it / kStages) & 1) ^ 1, ctl);
-          if (!good) set_abort(bar);
-          else if (aborted(bar)) good = false;
+          bool good = true;
+          if (Q4 && kb % kParGroups == 0) {
+            // scales and biases of groups kb .. kb + 7 of this tile's rows: each
+            // row's K / 8 code words are followed by its G scales, then G biases
+            // (bf16 columns K / 4 + g and K / 4 + G + g); with G = 4 one 8-wide
+            // box holds both
+            const int pb = pc & 1;
+            good = mbar_wait(&bar->pempty[pb], ((pc >> 1) & 1) ^ 1, ctl);
+            if (!good) set_abort(bar);
+            else if (aborted(bar)) good = false;
+            if (good) {
+              uint8_t* ps = par_buf + pb * 2 * kParBytes;
+              uint8_t* pbb = ps + kParBytes;
+              const int xs = K / 4 + kb, xb = K / 4 + G + kb;
+              const bool two = G >= kParGroups;
+              mbar_expect_tx(&bar->pfull[pb], (two ? 2 : 1) * kParBytes);
+              if (MODE == kGateUp) {
+                tma_load_2d_nohint(ps, mp, xs, brow0, &bar->pfull[pb]);
+                tma_load_2d_nohint(ps + kParBytes / 2, mp, xs, brow1, &bar->pfull[pb]);
+                if (two) {
+                  tma_load_2d_nohint(pbb, mp, xb, brow0, &bar->pfull[pb]);
+                  tma_load_2d_nohint(pbb + kParBytes / 2, mp, xb, brow1, &bar->pfull[pb]);
+                }
+              } else {
+                tma_load_2d_nohint(ps, mp, xs, brow0, &bar->pfull[pb]);
+                if (two) tma_load_2d_nohint(pbb, mp, xb, brow0, &bar->pfull[pb]);
+              }
+            }
+            ++pc;
+          }
+          if (good) {
+            good = mbar_wait(&bar->empty[st], ((it / S) & 1) ^ 1, ctl);
+            if (!good) set_abort(bar);
+            else if (aborted(bar)) good = false;
+          }
           if (good) {
             mbar_expect_tx(&bar->full[st], tx);
             uint8_t* a_dst = a_buf + st * kABytes;
-            uint8_t* b_dst = b_buf + st * kBBytes;
+            uint8_t* b_dst = Q4 ? raw_buf + st * kRawBytes : b_buf + st * kBBytes;
             const int kc = kb * kBK;
             const CUtensorMap* ma = MODE == kGateUp ? &maps.x_perm : (MODE == kDown ? &maps.h : &maps.x_tile);
             tma_load_2d(a_dst, ma, kc, wk.row0, &bar->full[st], pol_a);
-            if (MODE == kGateUp) {  // gate rows, then the up rows of the same neurons
+            if (Q4) {  // the k block's code words: 8 per row
+              if (MODE == kGateUp) {
+                tma_load_2d(b_dst, mb, kb * 8, brow0, &bar->full[st], pol_w);
+                tma_load_2d(b_dst + kRawBytes / 2, mb, kb * 8, brow1, &bar->full[st], pol_w);
+              } else {
+                tma_load_2d(b_dst, mb, kb * 8, brow0, &bar->full[st], pol_w);
+              }
+            } else if (MODE == kGateUp) {  // gate rows, then the up rows of the same neurons
               tma_load_2d(b_dst, mb, kc, brow0, &bar->full[st], pol_w);
               tma_load_2d(b_dst + 128 * 128, mb, kc, brow1, &bar->full[st], pol_w);
             } else {
@@ -184,8 +288,10 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
     }
     // drain: the copies into the last stages must land before the CTA exits
     if (lane == 0) {
-      const int n = min(it, kStages);
-      for (int j = it - n; j < it; ++j) mbar_wait(&bar->full[j % kStages], (j / kStages) & 1, drain);
+      const int n = min(it, S);
+      for (int j = it - n; j < it; ++j) mbar_wait(&bar->full[j % S], (j / S) & 1, drain);
+      if (Q4)
+        for (int j = max(0, pc - 2); j < pc; ++j) mbar_wait(&bar->pfull[j & 1], (j >> 1) & 1, drain);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
@@ -210,8 +316,9 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
         tc_fence_after();
         const uint32_t d_tmem = tmem + acc * kAccCols;
         for (int kb = 0; kb < KB; ++kb, ++it) {
-          const int st = it % kStages;
-          if (!mbar_wait(&bar->full[st], (it / kStages) & 1, ctl) || aborted(bar)) {
+          const int st = it % S;
+          // bf16: the stage's copies landed; 4-bit: the converters also expanded its B tile
+          if (!mbar_wait(Q4 ? &bar->conv[st] : &bar->full[st], (it / S) & 1, ctl) || aborted(bar)) {
             set_abort(bar);
             ok = false;
             break;
@@ -233,7 +340,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
       mbar_wait(&bar->mma_done, 0, drain);
     }
     __syncwarp();
-  } else {
+  } else if (warp < 6) {
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;               // TMEM lane quarter this warp may access
     const int row_local = q * 32 + lane;
@@ -296,6 +403,49 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
       tc_fence_before();
       mbar_arrive(&bar->tempty[acc]);
     }
+  } else if (Q4) {
+    // ------------------------------------------------------------ code expansion (4-bit)
+    // thread r expands B row r of every stage: its 8 code words (32 bytes of
+    // the raw tile) into 8 swizzled 16-byte chunks of bf16 weights
+    const int r = threadIdx.x - 6 * 32;
+    int it = 0, pc = 0;
+    bool ok = true;
+    for (int w = blockIdx.x; w < n_work && ok; w += gridDim.x) {
+      for (int kb = 0; kb < KB; ++kb, ++it) {
+        const int st = it % S, pb = pc & 1;  // pc: this k block's parameter load (already counted)
+        if (kb % kParGroups == 0) {
+          if (!mbar_wait(&bar->pfull[pb], (pc >> 1) & 1, ctl) || aborted(bar)) {
+            set_abort(bar);
+            ok = false;
+            break;
+          }
+        }
+        if (!mbar_wait(&bar->full[st], (it / S) & 1, ctl) || aborted(bar)) {
+          set_abort(bar);
+          ok = false;
+          break;
+        }
+        const uint16_t* ps = reinterpret_cast<const uint16_t*>(par_buf + pb * 2 * kParBytes);
+        const int g = kb % kParGroups;
+        const uint32_t sbits = ps[r * kParGroups + (G >= kParGroups ? g : kb)];
+        const uint32_t bbits = G >= kParGroups ? ps[kParBytes / 2 + r * kParGroups + g] : ps[r * kParGroups + G + kb];
+        const uint32_t s2 = sbits | (sbits << 16), b2 = bbits | (bbits << 16);
+        const uint4* raw = reinterpret_cast<const uint4*>(raw_buf + st * kRawBytes + r * 32);
+        const uint4 c0 = raw[0], c1 = raw[1];
+        uint8_t* row = b_buf + st * kBBytes + r * 128;
+        const uint32_t words[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+#pragma unroll
+        for (int c = 0; c < 8; ++c)
+          *reinterpret_cast<uint4*>(row + ((c ^ (r & 7)) << 4)) = expand_q4_word(words[c], s2, b2);
+        // the MMA reads the tile through the async proxy
+        fence_proxy_async_shared_cta();
+        mbar_arrive(&bar->conv[st]);
+        if (kb % kParGroups == kParGroups - 1 || kb == KB - 1) {
+          mbar_arrive(&bar->pempty[pb]);
+          ++pc;
+        }
+      }
+    }
   }
   tc_fence_before();
   __syncthreads();
@@ -309,18 +459,33 @@ static cudaError_t launch_mode(const Shapes& s, const GemmMaps& m, const Scratch
   DevCtl drain = ctl;
   drain.spin_limit = 2000000000LL;  // 2 s: copies and MMAs already issued always finish
   drain.stall = 0;
-  grouped_gemm_kernel<MODE><<<num_sms, kThreads, kSmemBytes, st>>>(m, s, sc, ctl, drain);
+  if (MODE != kRouter && s.q4)
+    grouped_gemm_kernel<MODE, true><<<num_sms, kThreadsQ4, kSmemBytesQ4, st>>>(m, s, sc, ctl, drain);
+  else
+    grouped_gemm_kernel<MODE, false><<<num_sms, kThreads, kSmemBytes, st>>>(m, s, sc, ctl, drain);
   return cudaGetLastError();
 }
 
 cudaError_t prepare_gemm_kernels() {
-  const void* ks[] = {(const void*)grouped_gemm_kernel<kGateUp>, (const void*)grouped_gemm_kernel<kDown>,
-                      (const void*)grouped_gemm_kernel<kRouter>};
+  const void* ks[] = {(const void*)grouped_gemm_kernel<kGateUp, false>, (const void*)grouped_gemm_kernel<kDown, false>,
+                      (const void*)grouped_gemm_kernel<kRouter, false>};
   for (const void* k : ks) {
     cudaError_t err = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
     if (err != cudaSuccess) return err;
   }
+  const void* kq[] = {(const void*)grouped_gemm_kernel<kGateUp, true>, (const void*)grouped_gemm_kernel<kDown, true>};
+  for (const void* k : kq) {
+    cudaError_t err = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytesQ4);
+    if (err != cudaSuccess) return err;
+  }
   return cudaSuccess;
+}
+
+// The 4-bit kernels' parameter loads need every weight row's K / 64 groups to
+// split into whole boxes of 8 (or to be exactly 4): K = 256 or K % 512 == 0.
+bool gemm_q4_supported(int d, int inter) {
+  auto ok = [](int K) { return K == 256 || K % 512 == 0; };
+  return ok(d) && ok(inter);
 }
 
 cudaError_t launch_gemm_gate_up(const Shapes& s, const GemmMaps& m, const Scratch& sc, const DevCtl& ctl,

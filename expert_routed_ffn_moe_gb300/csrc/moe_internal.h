@@ -58,6 +58,7 @@ struct Shapes {
   int x_bf16;             // 1: x is bf16, 0: fp32
   int bias_sel;           // 1: the router bias picks the experts but does not enter their weights
   int shared_gate;        // 1: the shared expert's output is scaled by sigmoid(x . g), g = router row E
+  int q4;                 // 1: expert weights are 4-bit group-affine (MOE_W_Q4G64 planes), 0: bf16
 };
 
 // moe_route.cu
@@ -93,8 +94,16 @@ struct GemmMaps {
   CUtensorMap down;         // experts [E*d, I], box 64 x 256
   CUtensorMap shared_down;  // shared down [d, I], box 64 x 256
   CUtensorMap wr_split;     // router weights hi/mid/lo [3E, d], box 64 x 256
+  // 4-bit weights (MOE_W_Q4G64 rows of 9 K / 16 bytes): each matrix seen twice,
+  // as uint32 words (the codes of a 64-column k block: box 8 x rows) and as
+  // bf16 (the scales / biases of 8 groups: box 8 x rows); no swizzle
+  CUtensorMap gu_codes, gu_params;      // routed gate_up [E 2I rows]
+  CUtensorMap sgu_codes, sgu_params;    // shared gate_up [2I rows]
+  CUtensorMap dn_codes, dn_params;      // routed down [E d rows]
+  CUtensorMap sdn_codes, sdn_params;    // shared down [d rows]
 };
 cudaError_t prepare_gemm_kernels();
+bool gemm_q4_supported(int d, int inter);
 cudaError_t launch_gemm_gate_up(const Shapes& s, const GemmMaps& m, const Scratch& sc, const DevCtl& ctl,
                                 int num_sms, cudaStream_t st);
 cudaError_t launch_gemm_down(const Shapes& s, const GemmMaps& m, const Scratch& sc, const DevCtl& ctl,

@@ -60,6 +60,23 @@ extern "C" {
 #define MOE_F32 0
 #define MOE_BF16 1
 
+/* storage format of the expert weights (moe_config.weight_format) */
+#define MOE_W_BF16 0           /* bf16 matrices, as described at moe_forward */
+#define MOE_W_Q4G64 1          /* 4-bit group-affine ("Optimizing on-device inference for Apple Silicon",
+                                  section "Dequantizing weights during matrix multiplication": 4-bit
+                                  codes expanded inside the multiplication).  Along every weight row
+                                  [K input columns], each group of 64 consecutive columns has one bf16
+                                  scale s and one bf16 bias b, and w = s * q + b for the column's 4-bit
+                                  code q in 0..15.  Each row of K weights is stored as 9 K / 16 bytes:
+                                  its codes (K / 8 uint32 words, eight codes per word, the lowest
+                                  nibble is the lowest column), then its K / 64 bf16 scales, then its
+                                  K / 64 bf16 biases.  Matrices are these rows back to back, in the
+                                  bf16 layouts' row order: experts_gate_up [E, 2I] rows of d weights,
+                                  experts_down [E, d] rows of I weights, shared_w the shared gate_up
+                                  [2I] rows of d weights followed by its down [d] rows of I weights.
+                                  Needs inter % 256 == 0 (and, on the grouped-GEMM path, d and inter
+                                  each 256 or a multiple of 512). */
+
 /* execution path for the expert FFNs (moe_set_path) */
 #define MOE_PATH_AUTO 0        /* T <= 7: GEMV over the selected experts; otherwise grouped GEMM */
 #define MOE_PATH_GEMV 1        /* bandwidth-bound GEMV over the selected experts (small T only, else
@@ -90,6 +107,8 @@ typedef struct moe_config {
   int shared_gate;     /* 1 (with has_shared): sigmoid-gated shared expert -- router_w holds E + 1 rows,
                           row E being a gate vector g of d fp32 values, and the shared expert's output
                           for token t is scaled by sigmoid(x_t . g) (no bias); 0: weight one */
+  int weight_format;   /* MOE_W_BF16 or MOE_W_Q4G64: how experts_gate_up, experts_down and shared_w
+                          are stored */
 } moe_config;
 
 typedef struct moe_ctx moe_ctx;

@@ -155,6 +155,40 @@ def draw_expert_q4(w: Workload, layer: int, e: int):
             _q4_matrix(w.d, inter, w.seed, layer, _Q4, e + 1, 1))
 
 
+def draw_experts_q4(w: Workload, layer: int = 0, experts=None, threads: int = 16):
+    """Stacked 4-bit routed experts (``draw_expert_q4``) for ``experts`` (default all):
+    dict of gu_words [n, 2I, d/8] u32, gu_scales / gu_biases [n, 2I, d/64] bf16 bits,
+    dn_words [n, d, I/8], dn_scales / dn_biases [n, d, I/64]."""
+    ids = list(range(w.E)) if experts is None else [int(e) for e in experts]
+    n = len(ids)
+    out = dict(gu_words=np.empty((n, 2 * w.I, w.d // 8), np.uint32),
+               gu_scales=np.empty((n, 2 * w.I, w.d // 64), np.uint16),
+               gu_biases=np.empty((n, 2 * w.I, w.d // 64), np.uint16),
+               dn_words=np.empty((n, w.d, w.I // 8), np.uint32),
+               dn_scales=np.empty((n, w.d, w.I // 64), np.uint16),
+               dn_biases=np.empty((n, w.d, w.I // 64), np.uint16))
+
+    def one(j):
+        (gw, gs, gb), (dw, ds, db) = draw_expert_q4(w, layer, ids[j])
+        out["gu_words"][j], out["gu_scales"][j], out["gu_biases"][j] = gw, gs, gb
+        out["dn_words"][j], out["dn_scales"][j], out["dn_biases"][j] = dw, ds, db
+
+    with ThreadPoolExecutor(max(1, threads)) as ex:
+        list(ex.map(one, range(n)))
+    return out
+
+
+def pack_q4(words: np.ndarray, scales: np.ndarray, biases: np.ndarray) -> np.ndarray:
+    """The library's byte layout of 4-bit matrices (MOE_W_Q4G64): every row as
+    its code words, then its scales, then its biases (9 K / 16 bytes for K
+    columns), rows back to back.  Pure data movement (no arithmetic): words
+    [..., R, K/8] u32, scales and biases [..., R, K/64] bf16 bits -> uint8 [bytes]."""
+    rows = np.concatenate([np.ascontiguousarray(words).view(np.uint8),
+                           np.ascontiguousarray(scales).view(np.uint8),
+                           np.ascontiguousarray(biases).view(np.uint8)], axis=-1)
+    return np.ascontiguousarray(rows).ravel()
+
+
 def draw_experts(w: Workload, layer: int = 0, experts=None, threads: int = 16):
     """Stacked routed experts: gate_up [n, 2I, d] and down [n, d, I] bf16 bits.
 

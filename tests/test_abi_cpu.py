@@ -46,6 +46,8 @@ def _cfg(**kw):
     (dict(bias_select_only=2), moe.MOE_ERR_ARG),
     (dict(shared_gate=2), moe.MOE_ERR_ARG),
     (dict(shared_gate=1, has_shared=0), moe.MOE_ERR_ARG),
+    (dict(weight_format=2), moe.MOE_ERR_ARG),
+    (dict(weight_format=moe.MOE_W_Q4G64), moe.MOE_ERR_UNSUPPORTED),  # 4-bit needs inter % 256 == 0
 ])
 def test_init_rejects_bad_configs_before_any_device_call(lib, kw, code):
     h = ctypes.c_void_p()
@@ -75,3 +77,21 @@ def test_binding_config_matches_header():
     fields = re.findall(r"\bint\s+(\w+)\s*;", body)
     assert [n for n, _ in moe.moe_config._fields_] == fields
     assert all(t is ctypes.c_int for _, t in moe.moe_config._fields_)
+
+
+def test_q4_row_layout():
+    # MOE_W_Q4G64 (moe.h): each row is its code words, then its scales, then its biases
+    import numpy as np
+
+    import moe_workloads as mw
+
+    words = np.array([[0x76543210], [0xFEDCBA98]], dtype=np.uint32)  # 2 rows of 8 codes
+    scales = np.array([[0x3F80], [0x4000]], dtype=np.uint16)
+    biases = np.array([[0xBF80], [0xC000]], dtype=np.uint16)
+    b = mw.pack_q4(words, scales, biases)
+    assert b.dtype == np.uint8 and b.size == 2 * (4 + 2 + 2)
+    row0, row1 = b[:8], b[8:]
+    assert row0[:4].tolist() == [0x10, 0x32, 0x54, 0x76]  # little-endian word, nibble 0 lowest
+    assert row0[4:].view(np.uint16).tolist() == [0x3F80, 0xBF80]  # then its scale, then its bias
+    assert row1[:4].tolist() == [0x98, 0xBA, 0xDC, 0xFE]
+    assert row1[4:].view(np.uint16).tolist() == [0x4000, 0xC000]

@@ -61,3 +61,22 @@ def test_algorithmic_bytes_and_flops_per_unit():
     # the shared-gate variant adds its fp32 gate row to the router bytes
     c2 = bench.layer_costs(w, idx, shared_gate=True)
     assert c2["layer_bytes"] - c["layer_bytes"] == 2048 * 4
+
+
+def test_q4_bytes_and_plane_roundtrip():
+    import numpy as np
+
+    import moe_workloads as mw
+
+    # one 4-bit expert at d = 2048, I = 512: half a byte per weight + a bf16 scale and bias per 64
+    q4_expert = 3 * 2048 * 512 // 2 + 3 * 2048 * 512 // 64 * 4
+    assert bench.expert_matrix_bytes(1024, 2048, True) + bench.expert_matrix_bytes(2048, 512, True) == q4_expert
+    c = bench.layer_costs(mw.WORKLOADS["decode"], np.arange(8)[None, :] * 3, q4=True)
+    assert c["layer_bytes"] == 9 * q4_expert + 256 * 2048 * 4 + 2 * 2048 * 2
+    # the bench's plane reader inverts moe_workloads.pack_q4
+    w = mw.Workload("q4rt", T=1, d=512, E=3, I=256, I_s=256, k=2, cid=9)
+    q = mw.draw_experts_q4(w)
+    buf = mw.pack_q4(q["dn_words"], q["dn_scales"], q["dn_biases"])
+    words, scales, biases = bench.unpack_q4_planes(buf, w.E, w.d, w.I)
+    assert np.array_equal(words, q["dn_words"]) and np.array_equal(scales, q["dn_scales"])
+    assert np.array_equal(biases, q["dn_biases"])
