@@ -421,6 +421,7 @@ int moe_route(moe_ctx* ctx, const void* x, int T, const float* router_w, const f
   memset(&maps, 0, sizeof(maps));
   if (tensor) {
     if ((rc = make_map(ctx, &maps.x_tile, x, s.d, s.T, 64, 128)) != MOE_OK) return rc;
+    if ((rc = make_map(ctx, &maps.x_tile16, x, s.d, s.T, 64, 16)) != MOE_OK) return rc;
     if ((rc = make_map(ctx, &maps.wr_split, ctx->sc.wr_split, s.d, 3 * s.E, 64, 256)) != MOE_OK) return rc;
   }
   if ((rc = run_route(ctx, s, x, router_w, router_b, tensor, &maps, st)) != MOE_OK) return rc;
@@ -533,8 +534,11 @@ static int forward_one(moe_ctx* ctx, const void* x, int T, const float* router_w
   memset(&maps, 0, sizeof(maps));
   const uint64_t rows = (uint64_t)s.T * s.k + (s.has_shared ? s.T : 0);
   if (s.x_bf16 && (rc = make_map(ctx, &maps.x_tile, x, s.d, s.T, 64, 128)) != MOE_OK) return rc;
+  if (s.x_bf16 && (rc = make_map(ctx, &maps.x_tile16, x, s.d, s.T, 64, 16)) != MOE_OK) return rc;
   if ((rc = make_map(ctx, &maps.x_perm, ctx->sc.x_perm, s.d, rows, 64, 128)) != MOE_OK) return rc;
+  if ((rc = make_map(ctx, &maps.x_perm16, ctx->sc.x_perm, s.d, rows, 64, 16)) != MOE_OK) return rc;
   if ((rc = make_map(ctx, &maps.h, ctx->sc.h, s.I, rows, 64, 128)) != MOE_OK) return rc;
+  if ((rc = make_map(ctx, &maps.h16, ctx->sc.h, s.I, rows, 64, 16)) != MOE_OK) return rc;
   if ((rc = make_map(ctx, &maps.wr_split, ctx->sc.wr_split, s.d, 3 * s.E, 64, 256)) != MOE_OK) return rc;
   if (s.q4) {
     // 4-bit rows: the routed experts, and the shared expert's gate_up rows followed by its down rows

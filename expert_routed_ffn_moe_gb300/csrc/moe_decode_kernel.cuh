@@ -287,16 +287,17 @@ MOE_DEV float q4_one_plus(uint32_t w) {
   const uint32_t v = sh >= 0 ? (w << sh) : (w >> (-sh));
   return __uint_as_float((v & 0x00780000u) | 0x3F800000u);
 }
-// sum_i (1 + q_i / 16) a_i over the 8 codes of word w and a[0..7]
+// sum_i (1 + q_i / 16) a_i over the 8 codes of word w and a[0..7] (two
+// independent chains, so consecutive FMAs do not wait on each other)
 MOE_DEV float q4_dot8(uint32_t w, const float4 a0, const float4 a1) {
-  float r = q4_one_plus<0>(w) * a0.x;
+  float r = q4_one_plus<0>(w) * a0.x, t = q4_one_plus<4>(w) * a1.x;
   r = fmaf(q4_one_plus<1>(w), a0.y, r);
+  t = fmaf(q4_one_plus<5>(w), a1.y, t);
   r = fmaf(q4_one_plus<2>(w), a0.z, r);
+  t = fmaf(q4_one_plus<6>(w), a1.z, t);
   r = fmaf(q4_one_plus<3>(w), a0.w, r);
-  r = fmaf(q4_one_plus<4>(w), a1.x, r);
-  r = fmaf(q4_one_plus<5>(w), a1.y, r);
-  r = fmaf(q4_one_plus<6>(w), a1.z, r);
-  return fmaf(q4_one_plus<7>(w), a1.w, r);
+  t = fmaf(q4_one_plus<7>(w), a1.w, t);
+  return r + t;
 }
 // One word's share of a 4-bit row dot product: with sum_i (1 + q_i/16) a_i =
 // raw and sum_i a_i = as, sum_i (s q_i + b) a_i = 16 s raw + (b - 16 s) as.

@@ -35,8 +35,12 @@
 // loads each k block's raw codes (256 rows x 32 bytes) and, every 8 k blocks,
 // the rows' scales and biases of those 8 groups; 8 more warps expand the codes
 // to bf16, w = s q + b rounded once (bf16x2 fma), straight into the 128-byte
-// swizzled B tile the MMA reads, then release it to the MMA issuer.  3 stages
-// of (A 16 KB + B 32 KB + codes 8 KB) plus two 8 KB parameter buffers.
+// swizzled B tile the MMA reads, then release it to the MMA issuer.  The loads
+// run in a 5-stage ring of (A 16 KB + codes 8 KB) and the expanded B tiles in
+// a 2-stage ring of 32 KB, so that the copies in flight cover the memory
+// latency while expansion and MMA overlap (one 3-stage ring of A + codes + B
+// kept only 3 loads in flight and ran the gate/up GEMM 2.3 times slower than
+// its tensor time); plus two 8 KB parameter buffers.
 #include "moe_internal.h"
 
 namespace moe {
@@ -54,17 +58,21 @@ constexpr int kThreads = 192;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kAccCols = 256;
 // 4-bit weights
-constexpr int kStagesQ4 = 3;
+constexpr int kStagesQ4 = 5;                     // loads (A + codes) in flight
+constexpr int kBStagesQ4 = 2;                    // expanded B tiles
 constexpr int kRawBytes = kBRows * 32;           // one k block of codes: 256 rows x 8 words
 constexpr int kParGroups = 8;                    // groups (k blocks) per parameter load
 constexpr int kParBytes = kBRows * kParGroups * 2;  // scales (or biases) of 8 groups for 256 rows: 4 KB
 constexpr int kConvWarps = 8;                    // warps expanding codes (one B row per thread)
 constexpr int kThreadsQ4 = kThreads + kConvWarps * 32;
 
+constexpr int kMaxStages = kStagesQ4 > kStages ? kStagesQ4 : kStages;
+
 struct __align__(8) Barriers {
-  uint64_t full[kStages];
-  uint64_t empty[kStages];
-  uint64_t conv[kStages];    // 4-bit: the stage's B tile has been expanded
+  uint64_t full[kMaxStages];
+  uint64_t empty[kMaxStages];
+  uint64_t conv[kBStagesQ4];    // 4-bit: the B stage's tile has been expanded
+  uint64_t bempty[kBStagesQ4];  // 4-bit: the MMA is done with the B stage
   uint64_t pfull[2];         // 4-bit: parameter buffer loaded
   uint64_t pempty[2];        // 4-bit: parameter buffer consumed
   uint64_t tfull[2];
@@ -75,8 +83,9 @@ struct __align__(8) Barriers {
 };
 
 constexpr size_t kSmemBytes = 1024 /*align slack*/ + (size_t)kStages * (kABytes + kBBytes) + sizeof(Barriers);
-constexpr size_t kSmemBytesQ4 = 1024 + (size_t)kStagesQ4 * (kABytes + kBBytes + kRawBytes) + 2 * 2 * kParBytes +
-                                sizeof(Barriers);
+constexpr size_t kSmemBytesQ4 = 1024 + (size_t)kStagesQ4 * (kABytes + kRawBytes) + (size_t)kBStagesQ4 * kBBytes +
+                                2 * 2 * kParBytes + sizeof(Barriers);
+static_assert(kSmemBytesQ4 <= 227 * 1024 && kSmemBytes <= 227 * 1024, "shared memory of one CTA");
 
 // fma.rn.bf16x2: a * b + c per half, computed exactly and rounded once
 MOE_DEV uint32_t fma_bf16x2(uint32_t a, uint32_t b, uint32_t c) {
@@ -155,12 +164,13 @@ MOE_DEV void set_abort(Barriers* b) { *reinterpret_cast<volatile int*>(&b->abort
 template <int MODE, bool Q4>
 __global__ void __launch_bounds__(Q4 ? kThreadsQ4 : kThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ GemmMaps maps, Shapes s, Scratch sc, DevCtl ctl, DevCtl drain) {
-  constexpr int S = Q4 ? kStagesQ4 : kStages;
+  constexpr int S = Q4 ? kStagesQ4 : kStages;     // load ring (A, and B or codes)
+  constexpr int SB = Q4 ? kBStagesQ4 : kStages;   // B tiles the MMA reads (bf16: part of the load ring)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* a_buf = base;
   uint8_t* b_buf = base + S * kABytes;
-  uint8_t* raw_buf = b_buf + S * kBBytes;                  // Q4: codes of each stage
+  uint8_t* raw_buf = b_buf + SB * kBBytes;                 // Q4: codes of each load stage
   uint8_t* par_buf = raw_buf + (Q4 ? S * kRawBytes : 0);   // Q4: [2 buffers][scales | biases]
   Barriers* bar = reinterpret_cast<Barriers*>(par_buf + (Q4 ? 2 * 2 * kParBytes : 0));
 
@@ -175,7 +185,10 @@ __global__ void __launch_bounds__(Q4 ? kThreadsQ4 : kThreads, 1)
     for (int i = 0; i < S; ++i) {
       mbar_init(&bar->full[i], 1);
       mbar_init(&bar->empty[i], 1);
+    }
+    for (int i = 0; i < kBStagesQ4; ++i) {
       mbar_init(&bar->conv[i], kConvWarps * 32);
+      mbar_init(&bar->bempty[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bar->tfull[i], 1);
@@ -198,7 +211,7 @@ __global__ void __launch_bounds__(Q4 ? kThreadsQ4 : kThreads, 1)
     if (lane == 0) tma_prefetch_desc(MODE == kGateUp ? &maps.x_perm : (MODE == kDown ? &maps.h : &maps.x_tile));
     const uint64_t pol_w = policy_evict_normal();  // several m-tiles of one expert reuse its weights
     const uint64_t pol_a = policy_evict_last();
-    constexpr uint32_t tx = kABytes + (Q4 ? kRawBytes : kBBytes);
+    constexpr uint32_t tx_b = Q4 ? kRawBytes : kBBytes;
     int it = 0, pc = 0;
     bool ok = true;
     for (int w = blockIdx.x; w < n_work && ok; w += gridDim.x) {
@@ -259,12 +272,24 @@ __global__ void __launch_bounds__(Q4 ? kThreadsQ4 : kThreads, 1)
             else if (aborted(bar)) good = false;
           }
           if (good) {
-            mbar_expect_tx(&bar->full[st], tx);
+            // A: the whole 128-row tile, or, for a group with fewer rows, only
+            // the 16-row boxes that cover them (the MMA still multiplies 128
+            // rows; the rows not loaded hold stale finite values of an earlier
+            // tile, and the epilogue drops their outputs)
+            const int a_boxes = (wk.rows + 15) / 16;
+            const bool whole = a_boxes >= kBM / 16;
+            mbar_expect_tx(&bar->full[st], (whole ? kABytes : a_boxes * 16 * kBK * 2) + tx_b);
             uint8_t* a_dst = a_buf + st * kABytes;
             uint8_t* b_dst = Q4 ? raw_buf + st * kRawBytes : b_buf + st * kBBytes;
             const int kc = kb * kBK;
-            const CUtensorMap* ma = MODE == kGateUp ? &maps.x_perm : (MODE == kDown ? &maps.h : &maps.x_tile);
-            tma_load_2d(a_dst, ma, kc, wk.row0, &bar->full[st], pol_a);
+            if (whole) {
+              const CUtensorMap* ma = MODE == kGateUp ? &maps.x_perm : (MODE == kDown ? &maps.h : &maps.x_tile);
+              tma_load_2d(a_dst, ma, kc, wk.row0, &bar->full[st], pol_a);
+            } else {
+              const CUtensorMap* ma = MODE == kGateUp ? &maps.x_perm16 : (MODE == kDown ? &maps.h16 : &maps.x_tile16);
+              for (int i = 0; i < a_boxes; ++i)
+                tma_load_2d(a_dst + i * 16 * kBK * 2, ma, kc, wk.row0 + 16 * i, &bar->full[st], pol_a);
+            }
             if (Q4) {  // the k block's code words: 8 per row
               if (MODE == kGateUp) {
                 tma_load_2d(b_dst, mb, kb * 8, brow0, &bar->full[st], pol_w);
@@ -316,22 +341,25 @@ __global__ void __launch_bounds__(Q4 ? kThreadsQ4 : kThreads, 1)
         tc_fence_after();
         const uint32_t d_tmem = tmem + acc * kAccCols;
         for (int kb = 0; kb < KB; ++kb, ++it) {
-          const int st = it % S;
-          // bf16: the stage's copies landed; 4-bit: the converters also expanded its B tile
-          if (!mbar_wait(Q4 ? &bar->conv[st] : &bar->full[st], (it / S) & 1, ctl) || aborted(bar)) {
+          const int st = it % S, sb = it % SB;
+          // bf16: the stage's copies landed; 4-bit: the converters expanded the
+          // B tile (after the stage's copies landed)
+          if (!mbar_wait(Q4 ? &bar->conv[sb] : &bar->full[st], Q4 ? (it / SB) & 1 : (it / S) & 1, ctl) ||
+              aborted(bar)) {
             set_abort(bar);
             ok = false;
             break;
           }
           tc_fence_after();
           const uint64_t ad = umma_desc_sw128(smem_u32(a_buf + st * kABytes));
-          const uint64_t bd = umma_desc_sw128(smem_u32(b_buf + st * kBBytes));
+          const uint64_t bd = umma_desc_sw128(smem_u32(b_buf + sb * kBBytes));
 #pragma unroll
           for (int kk = 0; kk < kBK / 16; ++kk) {
             // +32 bytes per 16-element k step inside the 128-byte swizzled row
             umma_bf16(d_tmem, ad + 2 * kk, bd + 2 * kk, idesc, (kb | kk) ? 1u : 0u);
           }
           umma_commit(&bar->empty[st]);
+          if (Q4) umma_commit(&bar->bempty[sb]);
         }
         if (!ok) break;
         umma_commit(&bar->tfull[acc]);
@@ -412,7 +440,7 @@ __global__ void __launch_bounds__(Q4 ? kThreadsQ4 : kThreads, 1)
     bool ok = true;
     for (int w = blockIdx.x; w < n_work && ok; w += gridDim.x) {
       for (int kb = 0; kb < KB; ++kb, ++it) {
-        const int st = it % S, pb = pc & 1;  // pc: this k block's parameter load (already counted)
+        const int st = it % S, sb = it % SB, pb = pc & 1;  // pc: this k block's parameter load
         if (kb % kParGroups == 0) {
           if (!mbar_wait(&bar->pfull[pb], (pc >> 1) & 1, ctl) || aborted(bar)) {
             set_abort(bar);
@@ -420,7 +448,8 @@ __global__ void __launch_bounds__(Q4 ? kThreadsQ4 : kThreads, 1)
             break;
           }
         }
-        if (!mbar_wait(&bar->full[st], (it / S) & 1, ctl) || aborted(bar)) {
+        if (!mbar_wait(&bar->full[st], (it / S) & 1, ctl) || !mbar_wait(&bar->bempty[sb], ((it / SB) & 1) ^ 1, ctl) ||
+            aborted(bar)) {
           set_abort(bar);
           ok = false;
           break;
@@ -432,14 +461,14 @@ __global__ void __launch_bounds__(Q4 ? kThreadsQ4 : kThreads, 1)
         const uint32_t s2 = sbits | (sbits << 16), b2 = bbits | (bbits << 16);
         const uint4* raw = reinterpret_cast<const uint4*>(raw_buf + st * kRawBytes + r * 32);
         const uint4 c0 = raw[0], c1 = raw[1];
-        uint8_t* row = b_buf + st * kBBytes + r * 128;
+        uint8_t* row = b_buf + sb * kBBytes + r * 128;
         const uint32_t words[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
 #pragma unroll
         for (int c = 0; c < 8; ++c)
           *reinterpret_cast<uint4*>(row + ((c ^ (r & 7)) << 4)) = expand_q4_word(words[c], s2, b2);
         // the MMA reads the tile through the async proxy
         fence_proxy_async_shared_cta();
-        mbar_arrive(&bar->conv[st]);
+        mbar_arrive(&bar->conv[sb]);
         if (kb % kParGroups == kParGroups - 1 || kb == KB - 1) {
           mbar_arrive(&bar->pempty[pb]);
           ++pc;
