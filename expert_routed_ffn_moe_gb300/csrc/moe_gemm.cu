@@ -66,7 +66,7 @@ constexpr int kParBytes = kBRows * kParGroups * 2;  // scales (or biases) of 8 g
 constexpr int kConvWarps = 8;                    // warps expanding codes (one B row per thread)
 constexpr int kThreadsQ4 = kThreads + kConvWarps * 32;
 
-constexpr int kMaxStages = kStagesQ4 > kStages ? kStagesQ4 : kStages;
+constexpr int kMaxStages = 6;  // the deepest load ring (small-batch layout with 16-row A slots)
 
 struct __align__(8) Barriers {
   uint64_t full[kMaxStages];
@@ -83,9 +83,26 @@ struct __align__(8) Barriers {
 };
 
 constexpr size_t kSmemBytes = 1024 /*align slack*/ + (size_t)kStages * (kABytes + kBBytes) + sizeof(Barriers);
+// Small batches (every expert group, the shared one included, has at most
+// AROWS <= T rows): an A slot holds only AROWS rows (2 or 4 KB), which frees
+// shared memory for more weight stages in flight.  The MMA still reads 128 rows
+// from the slot's start; past the AROWS real rows it reads whatever shared
+// memory follows (later A slots, then B tiles) -- finite values whose output
+// rows the epilogue drops -- and the slots are laid out first so those reads
+// stay inside the CTA's shared memory.
+constexpr int small_a_stages(int arows) { return arows == 16 ? 6 : 5; }
+constexpr size_t small_a_smem(int arows) {
+  return 1024 + (size_t)small_a_stages(arows) * (arows * kBK * 2 + kBBytes) + sizeof(Barriers);
+}
 constexpr size_t kSmemBytesQ4 = 1024 + (size_t)kStagesQ4 * (kABytes + kRawBytes) + (size_t)kBStagesQ4 * kBBytes +
                                 2 * 2 * kParBytes + sizeof(Barriers);
 static_assert(kSmemBytesQ4 <= 227 * 1024 && kSmemBytes <= 227 * 1024, "shared memory of one CTA");
+static_assert(small_a_stages(16) <= kMaxStages && small_a_stages(32) <= kMaxStages && kStagesQ4 <= kMaxStages,
+              "barrier arrays");
+static_assert(small_a_smem(16) <= 227 * 1024 && small_a_smem(32) <= 227 * 1024, "shared memory of one CTA");
+// the MMA reads 128 rows (16 KB) from any small A slot: the last slot's read must end inside the ring
+static_assert((small_a_stages(16) - 1) * 16 * 128 + kABytes <= small_a_stages(16) * (16 * 128 + kBBytes), "A reads");
+static_assert((small_a_stages(32) - 1) * 32 * 128 + kABytes <= small_a_stages(32) * (32 * 128 + kBBytes), "A reads");
 
 // fma.rn.bf16x2: a * b + c per half, computed exactly and rounded once
 MOE_DEV uint32_t fma_bf16x2(uint32_t a, uint32_t b, uint32_t c) {
@@ -161,15 +178,18 @@ MOE_DEV void set_abort(Barriers* b) { *reinterpret_cast<volatile int*>(&b->abort
 
 // Q4: the B operand (weights) is expanded from 4-bit codes by the converter
 // warps 6 .. 6 + kConvWarps - 1 (gate/up and down modes only).
-template <int MODE, bool Q4>
+// AROWS (bf16 only): 0 = full 128-row A slots; 16 or 32 = the small-batch
+// layout above (valid only when T <= AROWS).
+template <int MODE, bool Q4, int AROWS = 0>
 __global__ void __launch_bounds__(Q4 ? kThreadsQ4 : kThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ GemmMaps maps, Shapes s, Scratch sc, DevCtl ctl, DevCtl drain) {
-  constexpr int S = Q4 ? kStagesQ4 : kStages;     // load ring (A, and B or codes)
-  constexpr int SB = Q4 ? kBStagesQ4 : kStages;   // B tiles the MMA reads (bf16: part of the load ring)
+  constexpr int S = Q4 ? kStagesQ4 : (AROWS ? small_a_stages(AROWS) : kStages);  // load ring (A, and B or codes)
+  constexpr int SB = Q4 ? kBStagesQ4 : S;          // B tiles the MMA reads (bf16: part of the load ring)
+  constexpr int kASlot = AROWS ? AROWS * kBK * 2 : kABytes;  // bytes per A slot
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* a_buf = base;
-  uint8_t* b_buf = base + S * kABytes;
+  uint8_t* b_buf = base + S * kASlot;
   uint8_t* raw_buf = b_buf + SB * kBBytes;                 // Q4: codes of each load stage
   uint8_t* par_buf = raw_buf + (Q4 ? S * kRawBytes : 0);   // Q4: [2 buffers][scales | biases]
   Barriers* bar = reinterpret_cast<Barriers*>(par_buf + (Q4 ? 2 * 2 * kParBytes : 0));
@@ -279,7 +299,7 @@ __global__ void __launch_bounds__(Q4 ? kThreadsQ4 : kThreads, 1)
             const int a_boxes = (wk.rows + 15) / 16;
             const bool whole = a_boxes >= kBM / 16;
             mbar_expect_tx(&bar->full[st], (whole ? kABytes : a_boxes * 16 * kBK * 2) + tx_b);
-            uint8_t* a_dst = a_buf + st * kABytes;
+            uint8_t* a_dst = a_buf + st * kASlot;
             uint8_t* b_dst = Q4 ? raw_buf + st * kRawBytes : b_buf + st * kBBytes;
             const int kc = kb * kBK;
             if (whole) {
@@ -351,7 +371,7 @@ __global__ void __launch_bounds__(Q4 ? kThreadsQ4 : kThreads, 1)
             break;
           }
           tc_fence_after();
-          const uint64_t ad = umma_desc_sw128(smem_u32(a_buf + st * kABytes));
+          const uint64_t ad = umma_desc_sw128(smem_u32(a_buf + st * kASlot));
           const uint64_t bd = umma_desc_sw128(smem_u32(b_buf + sb * kBBytes));
 #pragma unroll
           for (int kk = 0; kk < kBK / 16; ++kk) {
@@ -490,6 +510,10 @@ static cudaError_t launch_mode(const Shapes& s, const GemmMaps& m, const Scratch
   drain.stall = 0;
   if (MODE != kRouter && s.q4)
     grouped_gemm_kernel<MODE, true><<<num_sms, kThreadsQ4, kSmemBytesQ4, st>>>(m, s, sc, ctl, drain);
+  else if (MODE != kRouter && s.T <= 16)  // every group has at most T rows
+    grouped_gemm_kernel<MODE, false, 16><<<num_sms, kThreads, small_a_smem(16), st>>>(m, s, sc, ctl, drain);
+  else if (MODE != kRouter && s.T <= 32)
+    grouped_gemm_kernel<MODE, false, 32><<<num_sms, kThreads, small_a_smem(32), st>>>(m, s, sc, ctl, drain);
   else
     grouped_gemm_kernel<MODE, false><<<num_sms, kThreads, kSmemBytes, st>>>(m, s, sc, ctl, drain);
   return cudaGetLastError();
@@ -505,6 +529,18 @@ cudaError_t prepare_gemm_kernels() {
   const void* kq[] = {(const void*)grouped_gemm_kernel<kGateUp, true>, (const void*)grouped_gemm_kernel<kDown, true>};
   for (const void* k : kq) {
     cudaError_t err = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytesQ4);
+    if (err != cudaSuccess) return err;
+  }
+  const void* k16[] = {(const void*)grouped_gemm_kernel<kGateUp, false, 16>,
+                       (const void*)grouped_gemm_kernel<kDown, false, 16>};
+  for (const void* k : k16) {
+    cudaError_t err = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)small_a_smem(16));
+    if (err != cudaSuccess) return err;
+  }
+  const void* k32[] = {(const void*)grouped_gemm_kernel<kGateUp, false, 32>,
+                       (const void*)grouped_gemm_kernel<kDown, false, 32>};
+  for (const void* k : k32) {
+    cudaError_t err = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)small_a_smem(32));
     if (err != cudaSuccess) return err;
   }
   return cudaSuccess;
