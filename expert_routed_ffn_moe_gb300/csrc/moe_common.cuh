@@ -36,6 +36,19 @@ MOE_DEV uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 p = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&p);
 }
+// The 8 bf16 of a 16-byte chunk (columns 0..7) reordered as 0, 4, 1, 5, 2,
+// 6, 3, 7: the column order in which the 4-bit GEMM expands a code word (its
+// nibbles i and i + 4 come out as one bf16 pair), so that the A operands of
+// that GEMM are stored in the same order and no reordering is needed when the
+// weights are expanded (the k-sum does not depend on the order).
+MOE_DEV uint4 q4_chunk_order(uint4 v) {
+  uint4 r;
+  asm("prmt.b32 %0, %1, %2, 0x5410;" : "=r"(r.x) : "r"(v.x), "r"(v.z));
+  asm("prmt.b32 %0, %1, %2, 0x7632;" : "=r"(r.y) : "r"(v.x), "r"(v.z));
+  asm("prmt.b32 %0, %1, %2, 0x5410;" : "=r"(r.z) : "r"(v.y), "r"(v.w));
+  asm("prmt.b32 %0, %1, %2, 0x7632;" : "=r"(r.w) : "r"(v.y), "r"(v.w));
+  return r;
+}
 MOE_DEV float warp_sum(float v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);

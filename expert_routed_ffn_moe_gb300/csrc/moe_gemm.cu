@@ -110,22 +110,19 @@ MOE_DEV uint32_t fma_bf16x2(uint32_t a, uint32_t b, uint32_t c) {
   asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
   return d;
 }
-MOE_DEV uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
-  uint32_t d;
-  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
-  return d;
-}
 // The 8 weights of one code word (columns 8 c .. 8 c + 7 of the k block) as
-// bf16 s q + b.  A code q is made exact in bf16 as (128 + q) - 128: the bits
-// 0x4300 | q are the bf16 value 128 + q.  Nibbles i and i + 4 share a word
-// half-pair; prmt puts the columns back in order.
+// bf16 s q + b, in the column order 0, 4, 1, 5, 2, 6, 3, 7 (q4_chunk_order):
+// nibbles i and i + 4 come out as one bf16 pair, and the A operands (x_perm,
+// h) are stored in the same order, so no reordering is needed.  A code q is
+// made exact in bf16 as (128 + q) - 128: the bits 0x4300 | q are the bf16
+// value 128 + q.
 MOE_DEV uint4 expand_q4_word(uint32_t w, uint32_t s2, uint32_t b2) {
   constexpr uint32_t kMagic = 0x43004300u, kOne = 0x3F803F80u, kMinus128 = 0xC300C300u;
   const uint32_t v0 = fma_bf16x2(fma_bf16x2((w & 0x000F000Fu) | kMagic, kOne, kMinus128), s2, b2);          // cols 0, 4
   const uint32_t v1 = fma_bf16x2(fma_bf16x2(((w >> 4) & 0x000F000Fu) | kMagic, kOne, kMinus128), s2, b2);   // 1, 5
   const uint32_t v2 = fma_bf16x2(fma_bf16x2(((w >> 8) & 0x000F000Fu) | kMagic, kOne, kMinus128), s2, b2);   // 2, 6
   const uint32_t v3 = fma_bf16x2(fma_bf16x2(((w >> 12) & 0x000F000Fu) | kMagic, kOne, kMinus128), s2, b2);  // 3, 7
-  return make_uint4(prmt(v0, v1, 0x5410u), prmt(v2, v3, 0x5410u), prmt(v0, v1, 0x7632u), prmt(v2, v3, 0x7632u));
+  return make_uint4(v0, v1, v2, v3);
 }
 MOE_DEV void tma_load_2d_nohint(void* dst, const CUtensorMap* m, int c0, int c1, uint64_t* bar) {
   asm volatile(
@@ -417,7 +414,10 @@ __global__ void __launch_bounds__(Q4 ? kThreadsQ4 : kThreads, 1)
           if (live) {
             uint4* o = reinterpret_cast<uint4*>(dst + c * 32);
 #pragma unroll
-            for (int j = 0; j < 4; ++j) o[j] = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+            for (int j = 0; j < 4; ++j) {
+              const uint4 v = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+              o[j] = Q4 ? q4_chunk_order(v) : v;  // 4-bit: h is the down GEMM's A, in the expansion order
+            }
           }
         }
       } else if (MODE == kDown) {

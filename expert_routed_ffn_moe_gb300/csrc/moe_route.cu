@@ -387,7 +387,9 @@ __global__ void __launch_bounds__(256) group_scatter_kernel(Shapes s, Scratch sc
 // warp per token computes the grouped positions of its k picks (as above),
 // reads the token's x row once, and writes it, in bf16, to each of those rows
 // of x_perm and to its shared-expert row -- instead of a scatter kernel that
-// writes perm and a second pass that gathers x by perm.
+// writes perm and a second pass that gathers x by perm.  With 4-bit weights
+// each 8-column chunk is stored in the 4-bit GEMM's column order
+// (q4_chunk_order).
 template <bool XBF16>
 __global__ void __launch_bounds__(256) group_scatter_rows_kernel(Shapes s, const void* __restrict__ x, Scratch sc,
                                                                  DevCtl ctl) {
@@ -425,6 +427,7 @@ __global__ void __launch_bounds__(256) group_scatter_rows_kernel(Shapes s, const
           const float4 a = __ldg(src + 2 * pc), b = __ldg(src + 2 * pc + 1);
           v[i] = make_uint4(pack_bf16x2(a.x, a.y), pack_bf16x2(a.z, a.w), pack_bf16x2(b.x, b.y), pack_bf16x2(b.z, b.w));
         }
+        if (s.q4) v[i] = q4_chunk_order(v[i]);  // the 4-bit GEMM's expansion order
       }
     }
     for (int j = -1; j < s.k; ++j) {
