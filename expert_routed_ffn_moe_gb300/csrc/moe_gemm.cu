@@ -289,12 +289,15 @@ __global__ void __launch_bounds__(Q4 ? kThreadsQ4 : kThreads, 1)
             else if (aborted(bar)) good = false;
           }
           if (good) {
-            // A: the whole 128-row tile, or, for a group with fewer rows, only
-            // the 16-row boxes that cover them (the MMA still multiplies 128
-            // rows; the rows not loaded hold stale finite values of an earlier
-            // tile, and the epilogue drops their outputs)
+            // A: the whole 128-row tile, or, for a group of at most 64 rows,
+            // only the 16-row boxes that cover them (the MMA still multiplies
+            // 128 rows; the rows not loaded hold stale finite values of an
+            // earlier tile, and the epilogue drops their outputs).  Above 64
+            // rows the extra box loads cost the producer more than the bytes
+            // they save (the balanced T = 4096 gate/up GEMM: 229 -> 236 us
+            // with boxes up to 112 rows)
             const int a_boxes = (wk.rows + 15) / 16;
-            const bool whole = a_boxes >= kBM / 16;
+            const bool whole = AROWS == 0 && a_boxes > 4;
             mbar_expect_tx(&bar->full[st], (whole ? kABytes : a_boxes * 16 * kBK * 2) + tx_b);
             uint8_t* a_dst = a_buf + st * kASlot;
             uint8_t* b_dst = Q4 ? raw_buf + st * kRawBytes : b_buf + st * kBBytes;
@@ -405,12 +408,17 @@ __global__ void __launch_bounds__(Q4 ? kThreadsQ4 : kThreads, 1)
         uint16_t* dst = sc.h + (size_t)(wk.row0 + row_local) * s.I + wk.n0;
 #pragma unroll 1
         for (int c = 0; c < 4; ++c) {
-          float g[32], u[32];
-          tmem_ld32(taddr + c * 32, g);
-          tmem_ld32(taddr + 128 + c * 32, u);
+          // the gate and up columns of the chunk: both loads, then one wait
+          uint32_t gr[32], ur[32];
+          tmem_ld32_async(taddr + c * 32, gr);
+          tmem_ld32_async(taddr + 128 + c * 32, ur);
+          tmem_ld_wait();
           uint32_t pk[16];
 #pragma unroll
-          for (int j = 0; j < 16; ++j) pk[j] = pack_bf16x2(silu(g[2 * j]) * u[2 * j], silu(g[2 * j + 1]) * u[2 * j + 1]);
+          for (int j = 0; j < 16; ++j) {
+            const float g0 = __uint_as_float(gr[2 * j]), g1 = __uint_as_float(gr[2 * j + 1]);
+            pk[j] = pack_bf16x2(silu(g0) * __uint_as_float(ur[2 * j]), silu(g1) * __uint_as_float(ur[2 * j + 1]));
+          }
           if (live) {
             uint4* o = reinterpret_cast<uint4*>(dst + c * 32);
 #pragma unroll
@@ -423,16 +431,22 @@ __global__ void __launch_bounds__(Q4 ? kThreadsQ4 : kThreads, 1)
       } else if (MODE == kDown) {
         uint16_t* dst = sc.out + (size_t)(wk.row0 + row_local) * s.d + wk.n0;
 #pragma unroll 1
-        for (int c = 0; c < 8; ++c) {
-          float v[32];
-          tmem_ld32(taddr + c * 32, v);
-          uint32_t pk[16];
+        for (int c = 0; c < 8; c += 2) {
+          // two 32-column chunks per wait
+          uint32_t v0[32], v1[32];
+          tmem_ld32_async(taddr + c * 32, v0);
+          tmem_ld32_async(taddr + (c + 1) * 32, v1);
+          tmem_ld_wait();
+          uint32_t pk[32];
 #pragma unroll
-          for (int j = 0; j < 16; ++j) pk[j] = pack_bf16x2(v[2 * j], v[2 * j + 1]);
+          for (int j = 0; j < 16; ++j) {
+            pk[j] = pack_bf16x2(__uint_as_float(v0[2 * j]), __uint_as_float(v0[2 * j + 1]));
+            pk[16 + j] = pack_bf16x2(__uint_as_float(v1[2 * j]), __uint_as_float(v1[2 * j + 1]));
+          }
           if (live) {
             uint4* o = reinterpret_cast<uint4*>(dst + c * 32);
 #pragma unroll
-            for (int j = 0; j < 4; ++j) o[j] = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+            for (int j = 0; j < 8; ++j) o[j] = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
           }
         }
       } else {

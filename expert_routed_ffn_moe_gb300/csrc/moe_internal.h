@@ -94,8 +94,8 @@ struct GemmMaps {
   CUtensorMap down;         // experts [E*d, I], box 64 x 256
   CUtensorMap shared_down;  // shared down [d, I], box 64 x 256
   CUtensorMap wr_split;     // router weights hi/mid/lo [3E, d], box 64 x 256
-  // the same A operands in boxes of 16 rows: a tile whose group has fewer than
-  // 113 rows loads only the boxes that cover its rows
+  // the same A operands in boxes of 16 rows: a tile whose group has at most
+  // 64 rows loads only the boxes that cover its rows
   CUtensorMap x_tile16, x_perm16, h16;
   // 4-bit weights (MOE_W_Q4G64 rows of 9 K / 16 bytes): each matrix seen twice,
   // as uint32 words (the codes of a 64-column k block: box 8 x rows) and as
