@@ -64,8 +64,8 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "expert_routed_ffn_moe_gb300", "csrc")
 # sources that decide each dominant kernel's code (its traffic record is void once they change)
 KERNEL_SOURCES = {
-    "decode_fused_kernel": ["moe_decode_kernel.cuh", "moe_decode.cu", "moe_decode_k1.cu", "moe_common.cuh",
-                            "moe_internal.h"],
+    "decode_fused_kernel": ["moe_decode_kernel.cuh", "moe_decode.cu", "moe_decode_k1.cu", "moe_decode_q4_k1.cu",
+                            "moe_common.cuh", "moe_internal.h"],
     "grouped_gemm_kernel<gate_up>": ["moe_gemm.cu", "moe_common.cuh", "moe_internal.h"],
 }
 

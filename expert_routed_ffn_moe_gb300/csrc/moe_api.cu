@@ -44,10 +44,10 @@ namespace {
 
 constexpr long long kDefaultSpinNs = 1000000000LL;  // 1 s
 // Largest T the automatic path sends to the small-T kernels.  Measured per layer (d = 2048, 256
-// experts, inter 512, top-8 + shared; fused kernel vs grouped GEMMs): T = 1: 19 vs 71 us, 2: 31 vs 82,
-// 3: 45 vs 88, 4: 61 vs 86, 5: 80 vs 117, 6: 102 vs 121, 7: 122 vs 123, 8: 130 vs 126 -- the GEMMs
-// win from T = 8.
-constexpr int kGemvMaxT = 7;
+// experts, inter 512, top-8 + shared, bf16; fused kernel vs grouped GEMMs, us): T = 1: 19.2 vs 46.8,
+// 2: 31.5 vs 52.5, 3: 45.5 vs 58.9, 4: 62.1 vs 65.5, 5: 79.4 vs 78.6, 6: 98.3 vs 86.2, 7: 129.1 vs
+// 89.2 -- the GEMMs tie at T = 5 and win beyond.
+constexpr int kGemvMaxT = 4;
 constexpr int kGemvSmemLimit = 200 * 1024;           // dynamic shared memory of the GEMV kernels
 constexpr int kDecodeReps = 8;                       // copies of the decode kernel's broadcast data
 

@@ -107,10 +107,16 @@ size_t decode_smem_bytes(const Shapes& s, int max_smem) {
   return decode_big_bytes(s) + (size_t)r.slots * r.slot_bytes;
 }
 
+// Below this ring depth every refill wave adds a memory round trip and the
+// kernel falls off a cliff (d = 2048, I = 512: T = 10 leaves a few slots and
+// took 480-800 us per layer, against ~110 us on the grouped GEMMs); such calls
+// go to the modular GEMV kernels instead.
+constexpr int kMinRingSlots = 6;
+
 bool decode_supported(const Shapes& s, int max_smem) {
   const void* k = decode_kernel_for(s);
   if (!(s.T <= 16 && s.d % 256 == 0 && s.I % 256 == 0 && k != nullptr)) return false;
-  return decode_ring(s, max_smem).slots >= 2;
+  return decode_ring(s, max_smem).slots >= kMinRingSlots;
 }
 
 cudaError_t prepare_decode_kernels(int max_smem) {

@@ -78,7 +78,7 @@ extern "C" {
                                   each 256 or a multiple of 512). */
 
 /* execution path for the expert FFNs (moe_set_path) */
-#define MOE_PATH_AUTO 0        /* T <= 7: GEMV over the selected experts; otherwise grouped GEMM */
+#define MOE_PATH_AUTO 0        /* T <= 4: GEMV over the selected experts; otherwise grouped GEMM */
 #define MOE_PATH_GEMV 1        /* bandwidth-bound GEMV over the selected experts (small T only, else
                                   MOE_ERR_UNSUPPORTED); for T <= 16 when shapes allow, the whole layer
                                   runs as one cooperative kernel whose blocks wait on each other's

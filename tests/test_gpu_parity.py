@@ -375,12 +375,14 @@ def test_shared_gate_needs_a_shared_expert():
         moe.MoeLayer(512, 64, 256, 4, 16, has_shared=False, shared_gate=True)
 
 
-@pytest.mark.parametrize("T", [2, 3, 4, 5, 7, 8, 10])
+@pytest.mark.parametrize("T", [2, 3, 4, 5, 7, 8, 9, 10, 11])
 def test_fused_kernel_each_token_bound(T):
     # the fused kernel is instantiated for token bounds 1, 2, 4, 8 and 16; run
     # each bound at the decode shapes (d = 2048, 256 experts, inter 512,
-    # top-8 + shared), at and between the bounds (T = 10 is the largest whose
-    # activations fit in shared memory at these shapes)
+    # top-8 + shared), at and between the bounds; the largest T here go to the
+    # modular GEMV kernels (the fused kernel needs a weight ring of at least 6
+    # slots beside its activations in shared memory; T = 11 is the GEMV
+    # kernels' limit at these shapes)
     full_case(mw.Workload(f"fused_T{T}", T=T, cid=91), path=moe.MOE_PATH_GEMV)
 
 
@@ -389,9 +391,9 @@ def test_fused_kernel_sixteen_tokens():
 
 
 def test_fused_kernel_rejects_tokens_beyond_shared_memory():
-    # T = 12 at the decode shapes: neither the fused kernel (up to T = 10
-    # here) nor the GEMV kernels (up to T = 11) hold its activations in
-    # shared memory; the forced small-T path says so
+    # T = 12 at the decode shapes: neither the fused kernel nor the GEMV
+    # kernels (up to T = 11) hold its activations in shared memory; the forced
+    # small-T path says so
     w = mw.Workload("fused_T12", T=12, cid=91)
     layer = make_layer(w, path=moe.MOE_PATH_GEMV)
     d = device_inputs(w, layer_inputs(w))
