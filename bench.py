@@ -67,6 +67,14 @@ KERNEL_SOURCES = {
     "decode_fused_kernel": ["moe_decode_kernel.cuh", "moe_decode.cu", "moe_decode_k1.cu", "moe_decode_q4_k1.cu",
                             "moe_common.cuh", "moe_internal.h"],
     "grouped_gemm_kernel<gate_up>": ["moe_gemm.cu", "moe_common.cuh", "moe_internal.h"],
+    # the other kernels of a layer (their records in profiles/ are evidence only; no line reads them)
+    "grouped_gemm_kernel<down>": ["moe_gemm.cu", "moe_common.cuh", "moe_internal.h"],
+    "grouped_gemm_kernel<router>": ["moe_gemm.cu", "moe_common.cuh", "moe_internal.h"],
+    "router_split_kernel": ["moe_route.cu", "moe_common.cuh", "moe_internal.h"],
+    "select_kernel": ["moe_route.cu", "moe_common.cuh", "moe_internal.h"],
+    "group_scan_kernel": ["moe_route.cu", "moe_common.cuh", "moe_internal.h"],
+    "group_scatter_rows_kernel": ["moe_route.cu", "moe_common.cuh", "moe_internal.h"],
+    "combine_kernel": ["moe_combine.cu", "moe_common.cuh", "moe_internal.h"],
 }
 
 
