@@ -493,38 +493,6 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const DecodeA
       }
       __syncthreads();
     }
-    // shared-expert gate/up + SwiGLU: item q < n_sh goes to warp kWarps - 1 - (q
-    // mod kWarps), the last warps, so that the selection warps of phase B (warp
-    // t for token t) start polling the logits while these units are computed
-    for (int q = kWarps - 1 - warp; q < n_sh; q += kWarps) {
-      const int slot = q % A.ring_slots;
-      if (!wait_item(full, slot_issued, q, A.ring_slots, A.ctl)) {
-        flag_s = 0;
-        break;
-      }
-      const int i = b + q * G;
-      const uint2* grow = reinterpret_cast<const uint2*>(ring + (size_t)slot * A.slot_bytes) + lane;
-      const uint2* urow = grow + s.d / 4;
-      for (int t = 0; t < s.T; ++t) {
-        float g = 0.f, up = 0.f;
-        if (Q4) {
-          q4_unit_dot<NCH>(ring + (size_t)slot * A.slot_bytes, s.d, big + (size_t)t * s.d,
-                           big + (size_t)s.T * s.d + (size_t)t * (s.d / 8), lane, g, up);
-        } else {
-          const float4* xr = reinterpret_cast<const float4*>(big + (size_t)t * s.d) + lane;
-#pragma unroll
-          for (int c = 0; c < 2 * NCH; ++c) dot4x2(grow[32 * c], urow[32 * c], xr[32 * c], g, up);
-        }
-        g = warp_sum(g);
-        up = warp_sum(up);
-        if (lane < sc.dec_hreps) st_tagged(dh + (size_t)lane * hrep + ((size_t)tk + t) * s.I + i, silu(g) * up, ep_s);
-      }
-      __syncwarp();  // every lane has read the slot
-      if (lane == 0 && q + A.ring_slots < n_sh) {  // later items need the routing: phase B issues them
-        fence_proxy_async_smem();
-        issue_item(A, q + A.ring_slots, slot, n_sh, 0, 1, b, G, 0, nullptr, ring, full, slot_issued);
-      }
-    }
   }
 
   // ---------------------------------------------------------------- phase B
@@ -710,11 +678,45 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(const DecodeA
     const int nr = (s.d > b) ? (s.d - b + G - 1) / G : 0;
     const int nch = (n_act + A.chunk_experts - 1) / A.chunk_experts;
     n_items = n_sh + nu + nr * nch;
-    // every slot is free (phase A consumed its items): fill all of them
+    // the slots past the shared expert's items are free: fill them (each
+    // shared item's slot is refilled by the warp that consumes it, below)
     if (warp == 0) {
-      if (lane < S) fence_proxy_async_smem();  // after the phase-A reads of the slots, before the copies overwrite them
-      for (int q = n_sh + lane; q < n_sh + S && q < n_items; q += 32)
-        issue_item(A, q, q % S, n_sh, nu, nch, b, G, n_act, act_e, ring, full, slot_issued);
+      for (int q = n_sh + lane; q < S && q < n_items; q += 32)
+        issue_item(A, q, q, n_sh, nu, nch, b, G, n_act, act_e, ring, full, slot_issued);
+    }
+    // shared-expert gate/up + SwiGLU, from rows that landed during the
+    // selection: item q < n_sh goes to warp kWarps - 1 - (q mod kWarps), the
+    // last warps, which have one routed unit fewer.  Computed beside the
+    // selection, their shared-memory loads took the issue slots of the pipe
+    // the selection's warp reductions use, and the selection ran 1.5 us.
+    for (int q = kWarps - 1 - warp; q < n_sh; q += kWarps) {
+      const int slot = q % S;
+      if (!wait_item(full, slot_issued, q, S, A.ctl)) {
+        flag_s = 0;
+        break;
+      }
+      const int i = b + q * G;
+      const uint2* grow = reinterpret_cast<const uint2*>(ring + (size_t)slot * A.slot_bytes) + lane;
+      const uint2* urow = grow + s.d / 4;
+      for (int t = 0; t < s.T; ++t) {
+        float g = 0.f, up = 0.f;
+        if (Q4) {
+          q4_unit_dot<NCH>(ring + (size_t)slot * A.slot_bytes, s.d, big + (size_t)t * s.d,
+                           big + (size_t)s.T * s.d + (size_t)t * (s.d / 8), lane, g, up);
+        } else {
+          const float4* xr = reinterpret_cast<const float4*>(big + (size_t)t * s.d) + lane;
+#pragma unroll
+          for (int c = 0; c < 2 * NCH; ++c) dot4x2(grow[32 * c], urow[32 * c], xr[32 * c], g, up);
+        }
+        g = warp_sum(g);
+        up = warp_sum(up);
+        if (lane < sc.dec_hreps) st_tagged(dh + (size_t)lane * hrep + ((size_t)tk + t) * s.I + i, silu(g) * up, ep_s);
+      }
+      __syncwarp();  // every lane has read the slot
+      if (lane == 0 && q + S < n_items) {
+        fence_proxy_async_smem();
+        issue_item(A, q + S, slot, n_sh, nu, nch, b, G, n_act, act_e, ring, full, slot_issued);
+      }
     }
     if (MAXT == 1 && b == 0 && sc.counts != nullptr && tid >= 32 && tid < 32 + s.E) {
       // batch 1: the layer's grouping tables, for moe_last_routing (one row per
