@@ -83,51 +83,118 @@ MOE_DEV void key_cx(uint32_t& ka, int& ea, uint32_t& kb, int& eb) {
   eb = e1;
 }
 
+// The logit of expert e in the warp layout of warp_top_k (lane l holds experts
+// l, l + 32, ..., in u[0..7]); every lane may ask for its own e.
+MOE_DEV float warp_logit_of(const float (&u)[8], int e) {
+  const int src = e & 31, slot = e >> 5;
+  float r = 0.f;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const float x = __shfl_sync(0xffffffffu, u[i], src);
+    if (i == slot) r = x;
+  }
+  return r;
+}
+
 // Warp-wide top-k of one token's E <= 256 logits, lane l holding the logits of
 // experts l, l+32, ..., l+224 in v[0..7] (-inf past E).  Every lane sorts its
-// 8 (logit, expert) pairs; each of the k rounds takes the warp's largest head
-// with two warp reductions (value, then the lowest expert id among equal
-// values) and the winning lane pops it.  On return lane j < k holds pick j:
+// 8 experts; each of the k rounds takes the warp's largest head with one warp
+// reduction on a word that packs the value's order key with the expert id, and
+// the winning lane pops it.  When that key's truncation leaves the boundary
+// between the k-th and (k+1)-th values undecided, the k rounds are redone with
+// two warp reductions each on the exact values (value, then the lowest expert
+// id among equal values).  Ties always go to the lower expert id.  On return lane j < k holds pick j:
 // its expert id, its weight exp(l_j - l_max) / sum over the picks (the softmax
 // over all E renormalised over the picks, common denominator cancelled) and its
 // rank in ascending expert id.  Returns false if some pick was not a number.
 MOE_DEV bool warp_top_k(const float (&v)[8], int E, int k, int lane, int& pick_e, float& pick_w, int& pick_rank) {
-  uint32_t kk[8];
-  int ee[8];
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const int e = lane + 32 * i;
-    ee[i] = e < E ? e : 0x7fffffff;
-    kk[i] = e < E ? ordered_key(v[i]) : 0u;
-  }
-  key_cx(kk[0], ee[0], kk[1], ee[1]); key_cx(kk[2], ee[2], kk[3], ee[3]);
-  key_cx(kk[4], ee[4], kk[5], ee[5]); key_cx(kk[6], ee[6], kk[7], ee[7]);
-  key_cx(kk[0], ee[0], kk[2], ee[2]); key_cx(kk[1], ee[1], kk[3], ee[3]);
-  key_cx(kk[4], ee[4], kk[6], ee[6]); key_cx(kk[5], ee[5], kk[7], ee[7]);
-  key_cx(kk[1], ee[1], kk[2], ee[2]); key_cx(kk[5], ee[5], kk[6], ee[6]);
-  key_cx(kk[0], ee[0], kk[4], ee[4]); key_cx(kk[1], ee[1], kk[5], ee[5]);
-  key_cx(kk[2], ee[2], kk[6], ee[6]); key_cx(kk[3], ee[3], kk[7], ee[7]);
-  key_cx(kk[2], ee[2], kk[4], ee[4]); key_cx(kk[3], ee[3], kk[5], ee[5]);
-  key_cx(kk[1], ee[1], kk[2], ee[2]); key_cx(kk[3], ee[3], kk[4], ee[4]); key_cx(kk[5], ee[5], kk[6], ee[6]);
   unsigned taken = 0u;  // bit i: this lane's expert lane + 32 i was picked
   int my_e = 0;
   float my_v = 0.f;
-  for (int r = 0; r < k; ++r) {
-    const uint32_t m = __reduce_max_sync(0xffffffffu, kk[0]);
-    const int emin = (int)__reduce_min_sync(0xffffffffu, (unsigned)(kk[0] == m ? ee[0] : 0x7fffffff));
-    if (ee[0] == emin) {
-      taken |= 1u << (emin >> 5);
+  bool done = false;
+  if (E <= 256) {
+    // One reduction per pick: a 32-bit word packs the order key's top 24 bits
+    // with 255 - expert id, so the largest word is the largest value and,
+    // among equal words, the lower id.  The picks are the exact top k when the
+    // k-th pick's 24-bit key is above every other expert's (the truncation is
+    // monotone); otherwise (a near-tie at the boundary, ~3e-4 of tokens) the
+    // exact rounds below decide.
+    uint32_t pk[8];
 #pragma unroll
-      for (int i = 0; i < 7; ++i) {
-        kk[i] = kk[i + 1];
-        ee[i] = ee[i + 1];
-      }
-      kk[7] = 0u;
-      ee[7] = 0x7fffffff;
+    for (int i = 0; i < 8; ++i) {
+      const int e = lane + 32 * i;
+      pk[i] = e < E ? ((ordered_key(v[i]) & 0xFFFFFF00u) | (uint32_t)(255 - e)) : 0u;
     }
-    if (lane == r) {
-      my_e = emin < E ? emin : r;
-      my_v = key_value(m);
+#define MOE_PK_CX(a, b)                  \
+  {                                      \
+    const uint32_t hi = max(pk[a], pk[b]); \
+    pk[b] = min(pk[a], pk[b]);           \
+    pk[a] = hi;                          \
+  }
+    MOE_PK_CX(0, 1) MOE_PK_CX(2, 3) MOE_PK_CX(4, 5) MOE_PK_CX(6, 7)
+    MOE_PK_CX(0, 2) MOE_PK_CX(1, 3) MOE_PK_CX(4, 6) MOE_PK_CX(5, 7)
+    MOE_PK_CX(1, 2) MOE_PK_CX(5, 6)
+    MOE_PK_CX(0, 4) MOE_PK_CX(1, 5) MOE_PK_CX(2, 6) MOE_PK_CX(3, 7)
+    MOE_PK_CX(2, 4) MOE_PK_CX(3, 5)
+    MOE_PK_CX(1, 2) MOE_PK_CX(3, 4) MOE_PK_CX(5, 6)
+#undef MOE_PK_CX
+    uint32_t mk = 0u;
+    for (int r = 0; r < k; ++r) {
+      const uint32_t m = __reduce_max_sync(0xffffffffu, pk[0]);
+      const int e = 255 - (int)(m & 0xFFu);
+      if ((e & 31) == lane) {
+        taken |= 1u << (e >> 5);
+#pragma unroll
+        for (int i = 0; i < 7; ++i) pk[i] = pk[i + 1];
+        pk[7] = 0u;
+      }
+      if (lane == r) my_e = e;
+      mk = m;
+    }
+    const uint32_t mn = k < E ? __reduce_max_sync(0xffffffffu, pk[0]) : 0u;
+    done = k >= E || (mk >> 8) > (mn >> 8);
+    if (done) {
+      my_v = warp_logit_of(v, my_e);
+    } else {
+      taken = 0u;
+      my_e = 0;
+    }
+  }
+  if (!done) {
+    uint32_t kk[8];
+    int ee[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int e = lane + 32 * i;
+      ee[i] = e < E ? e : 0x7fffffff;
+      kk[i] = e < E ? ordered_key(v[i]) : 0u;
+    }
+    key_cx(kk[0], ee[0], kk[1], ee[1]); key_cx(kk[2], ee[2], kk[3], ee[3]);
+    key_cx(kk[4], ee[4], kk[5], ee[5]); key_cx(kk[6], ee[6], kk[7], ee[7]);
+    key_cx(kk[0], ee[0], kk[2], ee[2]); key_cx(kk[1], ee[1], kk[3], ee[3]);
+    key_cx(kk[4], ee[4], kk[6], ee[6]); key_cx(kk[5], ee[5], kk[7], ee[7]);
+    key_cx(kk[1], ee[1], kk[2], ee[2]); key_cx(kk[5], ee[5], kk[6], ee[6]);
+    key_cx(kk[0], ee[0], kk[4], ee[4]); key_cx(kk[1], ee[1], kk[5], ee[5]);
+    key_cx(kk[2], ee[2], kk[6], ee[6]); key_cx(kk[3], ee[3], kk[7], ee[7]);
+    key_cx(kk[2], ee[2], kk[4], ee[4]); key_cx(kk[3], ee[3], kk[5], ee[5]);
+    key_cx(kk[1], ee[1], kk[2], ee[2]); key_cx(kk[3], ee[3], kk[4], ee[4]); key_cx(kk[5], ee[5], kk[6], ee[6]);
+    for (int r = 0; r < k; ++r) {
+      const uint32_t m = __reduce_max_sync(0xffffffffu, kk[0]);
+      const int emin = (int)__reduce_min_sync(0xffffffffu, (unsigned)(kk[0] == m ? ee[0] : 0x7fffffff));
+      if (ee[0] == emin) {
+        taken |= 1u << (emin >> 5);
+#pragma unroll
+        for (int i = 0; i < 7; ++i) {
+          kk[i] = kk[i + 1];
+          ee[i] = ee[i + 1];
+        }
+        kk[7] = 0u;
+        ee[7] = 0x7fffffff;
+      }
+      if (lane == r) {
+        my_e = emin < E ? emin : r;
+        my_v = key_value(m);
+      }
     }
   }
   const bool finite = !(lane < k && !(my_v == my_v && my_v > -INFINITY));
@@ -136,7 +203,8 @@ MOE_DEV bool warp_top_k(const float (&v)[8], int E, int k, int lane, int& pick_e
   // check allows 1e-5); with k <= 8 the picks sit in lanes 0..7, so three
   // butterfly steps sum them (measured on one warp: the accurate expf, divide
   // and 5-step sum took ~590 of the ~1800 cycles of a top-8 selection)
-  const float vmax = __shfl_sync(0xffffffffu, my_v, 0);
+  float vmax = lane < k ? my_v : -INFINITY;
+  for (int o = k <= 8 ? 4 : 16; o > 0; o >>= 1) vmax = fmaxf(vmax, __shfl_xor_sync(0xffffffffu, vmax, o));
   const float ex = lane < k ? __expf(my_v - vmax) : 0.f;
   float den = ex;
   for (int o = k <= 8 ? 4 : 16; o > 0; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
@@ -153,19 +221,6 @@ MOE_DEV bool warp_top_k(const float (&v)[8], int E, int k, int lane, int& pick_e
   pick_w = __fdividef(ex, den);
   pick_rank = rank;
   return __all_sync(0xffffffffu, finite);
-}
-
-// The logit of expert e in the warp layout of warp_top_k (lane l holds experts
-// l, l + 32, ..., in u[0..7]); every lane may ask for its own e.
-MOE_DEV float warp_logit_of(const float (&u)[8], int e) {
-  const int src = e & 31, slot = e >> 5;
-  float r = 0.f;
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const float x = __shfl_sync(0xffffffffu, u[i], src);
-    if (i == slot) r = x;
-  }
-  return r;
 }
 
 // Weights of the picks from other logits than the ones that chose them (a

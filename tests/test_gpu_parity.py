@@ -401,3 +401,20 @@ def test_fused_kernel_rejects_tokens_beyond_shared_memory():
         layer.forward(d["x"], d["router_w"], d["router_b"], d["gate_up"], d["down"], d["shared"])
     assert e.value.code == moe.MOE_ERR_UNSUPPORTED
     layer.close()
+
+
+@pytest.mark.parametrize("T,path,router", [(1, moe.MOE_PATH_GEMV, moe.MOE_ROUTER_AUTO),
+                                           (3, moe.MOE_PATH_GEMV, moe.MOE_ROUTER_AUTO),
+                                           (64, moe.MOE_PATH_GEMM, moe.MOE_ROUTER_AUTO),
+                                           (200, moe.MOE_PATH_GEMM, moe.MOE_ROUTER_TENSOR),
+                                           (200, moe.MOE_PATH_GEMM, moe.MOE_ROUTER_SIMT)])
+def test_exact_ties_go_to_the_lower_expert(T, path, router):
+    # Router rows repeat with period 4 (expert e gets row e mod 4), so a
+    # token's 256 logits take 4 values, each shared by 64 experts: the top-8
+    # boundary always falls inside an exact tie, which the selection must break
+    # toward the lower expert ids as the oracle does.  (The one-reduction-per-
+    # pick rounds cannot decide such a boundary; the exact rounds must run.)
+    w = custom(f"ties_T{T}", T=T, d=512, E=256, I=256, I_s=256, k=8, cid=97)
+    inp = layer_inputs(w, 0)
+    inp = dict(inp, router_w=np.ascontiguousarray(inp["router_w"][np.arange(w.E) % 4]))
+    full_case(w, path=path, router=router, inp=inp)
