@@ -15,13 +15,17 @@ from concurrent.futures import ThreadPoolExecutor
 PKG = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
-BUILD = os.path.join(PKG, "_build")
-LIB = os.path.join(PKG, "libmoe_gb300.so")
+# MOE_DEBUG_CHECKS=1 in the environment selects the build with the device
+# bounds checks of the grouping tables' entries (-DMOE_DEBUG_CHECKS), kept in
+# its own build folder and library; the package then loads that library.
+DEBUG_CHECKS = os.environ.get("MOE_DEBUG_CHECKS") == "1"
+BUILD = os.path.join(PKG, "_build_debug" if DEBUG_CHECKS else "_build")
+LIB = os.path.join(PKG, "libmoe_gb300_debug.so" if DEBUG_CHECKS else "libmoe_gb300.so")
 INCLUDE = os.path.join(ROOT, "include")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 CFLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
-          "-Xptxas", "-warn-spills"]
+          "-Xptxas", "-warn-spills"] + (["-DMOE_DEBUG_CHECKS"] if DEBUG_CHECKS else [])
 
 
 def nvcc() -> str:

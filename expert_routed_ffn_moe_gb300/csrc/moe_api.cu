@@ -5,6 +5,8 @@
 #include <stdlib.h>
 #include <string.h>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "moe_internal.h"
 
 using namespace moe;
@@ -154,8 +156,32 @@ cudaError_t record_event(cudaEvent_t ev, cudaStream_t st) {
   return cudaEventRecordWithFlags(ev, st, cs == cudaStreamCaptureStatusActive ? cudaEventRecordExternal : 0u);
 }
 
+// An NVTX range over a scope.
+struct NvtxRange {
+  explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+  ~NvtxRange() { nvtxRangePop(); }
+};
+
+// NVTX range names of the launches (a profiler shows each launch's host call
+// under its step of the layer; header-only NVTX costs nothing without a tool)
+const char* range_name(int id) {
+  switch (id) {
+    case -2: return "moe.router_split";
+    case MOE_K_ROUTER: return "moe.router";
+    case MOE_K_SELECT: return "moe.select";
+    case MOE_K_GROUP: return "moe.group";
+    case MOE_K_GEMV_GATE_UP: return "moe.gemv_gate_up";
+    case MOE_K_GEMV_DOWN: return "moe.gemv_down";
+    case MOE_K_GEMM_GATE_UP: return "moe.gemm_gate_up";
+    case MOE_K_GEMM_DOWN: return "moe.gemm_down";
+    case MOE_K_COMBINE: return "moe.combine";
+    case MOE_K_DECODE_FUSED: return "moe.decode_fused";
+    default: return "moe.kernel";
+  }
+}
+
 template <typename F>
-cudaError_t launch(moe_ctx* ctx, int id, cudaStream_t st, F&& f) {
+cudaError_t launch_timed(moe_ctx* ctx, int id, cudaStream_t st, F&& f) {
   const bool timed = ctx->timed_kernel == id;
   if (timed) {
     cudaError_t e = record_event(ctx->ev_start, st);
@@ -168,6 +194,12 @@ cudaError_t launch(moe_ctx* ctx, int id, cudaStream_t st, F&& f) {
     ctx->timed_kernel = -1;
   }
   return err;
+}
+
+template <typename F>
+cudaError_t launch(moe_ctx* ctx, int id, cudaStream_t st, F&& f) {
+  const NvtxRange range(range_name(id));
+  return launch_timed(ctx, id, st, f);
 }
 
 // Steps 1-4 on the device: logits, selection, grouping.
@@ -464,6 +496,7 @@ int moe_forward(moe_ctx* ctx, const void* x, int T, const float* router_w, const
                 const void* experts_gate_up, const void* experts_down, const void* shared_w, int top_k, void* y,
                 void* stream) {
   if (!ctx || T < 0) return MOE_ERR_ARG;
+  const NvtxRange range("moe_forward");
   const int chunk = ctx->chunk;
   if (chunk == 0 || T <= chunk)
     return forward_one(ctx, x, T, router_w, router_b, experts_gate_up, experts_down, shared_w, top_k, y, stream);

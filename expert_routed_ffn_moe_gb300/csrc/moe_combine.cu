@@ -46,6 +46,10 @@ __global__ void __launch_bounds__(256) combine_kernel(Shapes s, void* __restrict
     for (int u = 0; u < kRows; ++u) {
       const bool in = j0 + u < s.k;
       p[u] = in ? sc.slot[(size_t)t * s.k + j0 + u] : 0;
+      if (kDebugChecks && (p[u] < 0 || p[u] >= s.T * s.k)) {
+        atomicOr(sc.status, kStatusBounds);
+        p[u] = 0;
+      }
       wj[u] = in ? sc.w[(size_t)t * s.k + j0 + u] : 0.f;
     }
     uint4 v[kRows];

@@ -29,6 +29,17 @@ struct DevCtl {
 
 MOE_DEV void raise_status(const DevCtl& c, unsigned bit) { atomicOr(c.status, bit); }
 
+// Bounds checks of the grouping tables' entries where kernels read them (the
+// grouped GEMMs' tile list, the combine's slots, the scatter's positions, the
+// fused decode kernel's active experts), compiled in with -DMOE_DEBUG_CHECKS:
+// a bad entry latches kStatusBounds and is replaced by a valid one, so no
+// access leaves its array (the output is then wrong and the status says so).
+#ifdef MOE_DEBUG_CHECKS
+constexpr bool kDebugChecks = true;
+#else
+constexpr bool kDebugChecks = false;
+#endif
+
 // ---------------------------------------------------------------- small math
 MOE_DEV float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
 MOE_DEV float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xffff0000u); }

@@ -158,6 +158,17 @@ MOE_DEV void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar,
 }
 MOE_DEV void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 
+// An active expert id before its rows are copied: a routed expert (and, for
+// down rows, the shared expert E); with MOE_DEBUG_CHECKS anything else latches
+// kStatusBounds and reads expert 0 instead.
+MOE_DEV int checked_expert(const DecodeArgs& A, int e, bool shared_ok) {
+  if (kDebugChecks && (e < 0 || e > A.s.E || (e == A.s.E && !(shared_ok && A.s.has_shared)))) {
+    raise_status(A.ctl, kStatusBounds);
+    return 0;
+  }
+  return e;
+}
+
 // Start the bulk copies of item q of this block's weight stream into `slot`
 // (one thread).  Items q < n_sh are the shared expert's gate/up units
 // i = b + q G: its gate row i and up row i, back to back.  The next nu items
@@ -184,7 +195,7 @@ MOE_DEV void issue_item(const DecodeArgs& A, int q, int slot, int n_sh, int nu, 
       } else {
         const int u = b + (q - n_sh) * G, a = u / s.I;
         i = u - a * s.I;
-        W = reinterpret_cast<const uint8_t*>(A.gate_up) + (size_t)act_e[a] * 2 * s.I * row;
+        W = reinterpret_cast<const uint8_t*>(A.gate_up) + (size_t)checked_expert(A, act_e[a], false) * 2 * s.I * row;
       }
       mbar_expect_tx(&full[slot], 2 * row);
       bulk_g2s(dst, W + (size_t)i * row, row, &full[slot], pol);
@@ -195,7 +206,7 @@ MOE_DEV void issue_item(const DecodeArgs& A, int q, int slot, int n_sh, int nu, 
       const uint32_t row = (uint32_t)s.I / 16 * 9;
       mbar_expect_tx(&full[slot], (uint32_t)na * row);
       for (int qa = 0; qa < na; ++qa) {
-        const int e = act_e[a0 + qa];
+        const int e = checked_expert(A, act_e[a0 + qa], true);
         const uint8_t* Wd = (e < s.E) ? reinterpret_cast<const uint8_t*>(A.down) + (size_t)e * s.d * row : A.sh_down_q4;
         bulk_g2s(dst + (size_t)qa * row, Wd + (size_t)r * row, row, &full[slot], pol);
       }
@@ -208,7 +219,7 @@ MOE_DEV void issue_item(const DecodeArgs& A, int q, int slot, int n_sh, int nu, 
     bulk_g2s(dst + row, A.shared_w + (size_t)(s.I + i) * s.d, row, &full[slot], pol);
   } else if ((q -= n_sh) < nu) {
     const int u = b + q * G, a = u / s.I, i = u - a * s.I;
-    const uint16_t* W = A.gate_up + (size_t)act_e[a] * 2 * s.I * s.d;
+    const uint16_t* W = A.gate_up + (size_t)checked_expert(A, act_e[a], false) * 2 * s.I * s.d;
     const uint32_t row = (uint32_t)s.d * 2;
     mbar_expect_tx(&full[slot], 2 * row);
     bulk_g2s(dst, W + (size_t)i * s.d, row, &full[slot], pol);
@@ -219,7 +230,7 @@ MOE_DEV void issue_item(const DecodeArgs& A, int q, int slot, int n_sh, int nu, 
     const uint32_t row = (uint32_t)s.I * 2;
     mbar_expect_tx(&full[slot], (uint32_t)na * row);
     for (int qa = 0; qa < na; ++qa) {
-      const int e = act_e[a0 + qa];
+      const int e = checked_expert(A, act_e[a0 + qa], true);
       const uint16_t* Wd = (e < s.E) ? A.down + (size_t)e * s.d * s.I : A.shared_w + (size_t)2 * s.I * s.d;
       bulk_g2s(dst + (size_t)qa * row, Wd + (size_t)r * s.I, row, &full[slot], pol);
     }

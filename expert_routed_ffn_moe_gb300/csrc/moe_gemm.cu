@@ -140,9 +140,13 @@ struct Work {
 
 template <int MODE>
 MOE_DEV int work_count(const Shapes& s, const Scratch& sc) {
-  if (MODE == kGateUp) return sc.meta[0] * (s.I / 128);
-  if (MODE == kDown) return sc.meta[0] * (s.d / 256);
-  return ((s.T + kBM - 1) / kBM) * 3;
+  if (MODE == kRouter) return ((s.T + kBM - 1) / kBM) * 3;
+  int n = sc.meta[0];
+  if (kDebugChecks && (n < 0 || n > sc.max_mtiles)) {
+    atomicOr(sc.status, kStatusBounds);
+    n = 0;
+  }
+  return n * (MODE == kGateUp ? s.I / 128 : s.d / 256);
 }
 
 template <int MODE>
@@ -159,7 +163,15 @@ MOE_DEV Work work_item(const Shapes& s, const Scratch& sc, int w) {
   }
   const int nnt = (MODE == kGateUp) ? s.I / 128 : s.d / 256;
   const int mt = w / nnt, nt = w - mt * nnt;
-  const MTile m = sc.mtiles[mt];
+  MTile m = sc.mtiles[mt];
+  if (kDebugChecks) {
+    const int total = s.T * s.k + (s.has_shared ? s.T : 0);  // grouped rows
+    if (m.e < 0 || m.e > s.E || (m.e == s.E && !s.has_shared) || m.rows < 1 || m.rows > kBM || m.row0 < 0 ||
+        m.row0 + m.rows > total) {
+      atomicOr(sc.status, kStatusBounds);
+      m = MTile{0, 0, 1, 0};  // every role of the kernel reads the same entry and replaces it alike
+    }
+  }
   r.e = m.e;
   r.row0 = m.row0;
   r.rows = m.rows;

@@ -374,6 +374,10 @@ __global__ void __launch_bounds__(256) group_scatter_kernel(Shapes s, Scratch sc
     }
     const unsigned m = sc.chunk_mask[(size_t)c * s.E + e];
     const int pos = sc.offsets[e] + sc.chunk_base[(size_t)e * nchunk + c] + __popc(m & ((1u << tl) - 1u));
+    if (kDebugChecks && (pos < 0 || pos >= s.T * s.k)) {
+      raise_status(ctl, kStatusBounds);
+      continue;
+    }
     sc.perm[pos] = t;
     sc.slot[(size_t)t * s.k + j] = pos;
   }
@@ -406,8 +410,13 @@ __global__ void __launch_bounds__(256) group_scatter_rows_kernel(Shapes s, const
     } else {
       const unsigned m = sc.chunk_mask[(size_t)c * s.E + e];
       pos = sc.offsets[e] + sc.chunk_base[(size_t)e * nchunk + c] + __popc(m & ((1u << tl) - 1u));
-      sc.perm[pos] = t;
-      sc.slot[(size_t)t * s.k + lane] = pos;
+      if (kDebugChecks && (pos < 0 || pos >= s.T * s.k)) {
+        raise_status(ctl, kStatusBounds);
+        pos = -1;
+      } else {
+        sc.perm[pos] = t;
+        sc.slot[(size_t)t * s.k + lane] = pos;
+      }
     }
   }
   const long long shared_row = s.has_shared ? (long long)s.T * s.k + t : -1;
