@@ -327,6 +327,7 @@ int moe_init(const moe_config* cfg, moe_ctx** out) {
   const size_t o_perm = take(rows * 4);
   const size_t o_slot = take(T * k * 4);
   const size_t o_mtiles = take((size_t)max_mtiles * sizeof(MTile));
+  const size_t o_mpairs = take((size_t)max_mtiles * sizeof(MTile));
   const size_t o_meta = take(4 * 4);
   const size_t o_active = take((E + 1) * 4);
   const size_t o_tickets = take(4 * 4);
@@ -363,6 +364,7 @@ int moe_init(const moe_config* cfg, moe_ctx** out) {
   sc.perm = reinterpret_cast<int*>(b + o_perm);
   sc.slot = reinterpret_cast<int*>(b + o_slot);
   sc.mtiles = reinterpret_cast<MTile*>(b + o_mtiles);
+  sc.mpairs = reinterpret_cast<MTile*>(b + o_mpairs);
   sc.meta = reinterpret_cast<int*>(b + o_meta);
   sc.active = reinterpret_cast<int*>(b + o_active);
   sc.tickets = reinterpret_cast<unsigned*>(b + o_tickets);

@@ -58,7 +58,7 @@ constexpr int kThreads = 192;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kAccCols = 256;
 // 4-bit weights
-constexpr int kStagesQ4 = 5;                     // loads (A + codes) in flight
+constexpr int kStagesQ4 = 3;                     // loads (two A tiles + codes) in flight
 constexpr int kBStagesQ4 = 2;                    // expanded B tiles
 constexpr int kRawBytes = kBRows * 32;           // one k block of codes: 256 rows x 8 words
 constexpr int kParGroups = 8;                    // groups (k blocks) per parameter load
@@ -94,7 +94,7 @@ constexpr int small_a_stages(int arows) { return arows == 16 ? 6 : 5; }
 constexpr size_t small_a_smem(int arows) {
   return 1024 + (size_t)small_a_stages(arows) * (arows * kBK * 2 + kBBytes) + sizeof(Barriers);
 }
-constexpr size_t kSmemBytesQ4 = 1024 + (size_t)kStagesQ4 * (kABytes + kRawBytes) + (size_t)kBStagesQ4 * kBBytes +
+constexpr size_t kSmemBytesQ4 = 1024 + (size_t)kStagesQ4 * (2 * kABytes + kRawBytes) + (size_t)kBStagesQ4 * kBBytes +
                                 2 * 2 * kParBytes + sizeof(Barriers);
 static_assert(kSmemBytesQ4 <= 227 * 1024 && kSmemBytes <= 227 * 1024, "shared memory of one CTA");
 static_assert(small_a_stages(16) <= kMaxStages && small_a_stages(32) <= kMaxStages && kStagesQ4 <= kMaxStages,
@@ -134,14 +134,15 @@ MOE_DEV void tma_load_2d_nohint(void* dst, const CUtensorMap* m, int c0, int c1,
 
 struct Work {
   int e, row0, rows;   // expert (E = shared), first grouped row, valid rows
+  int rows2;           // 4-bit: valid rows of the pair's second tile (rows row0 + 128 ...; 0: none)
   int n0;              // first output column of the tile (B row offset inside the expert)
   int part;            // router: 0 / 1 / 2 = hi / mid / lo weight term
 };
 
-template <int MODE>
+template <int MODE, bool PAIRS = false>
 MOE_DEV int work_count(const Shapes& s, const Scratch& sc) {
   if (MODE == kRouter) return ((s.T + kBM - 1) / kBM) * 3;
-  int n = sc.meta[0];
+  int n = sc.meta[PAIRS ? 2 : 0];
   if (kDebugChecks && (n < 0 || n > sc.max_mtiles)) {
     atomicOr(sc.status, kStatusBounds);
     n = 0;
@@ -149,7 +150,7 @@ MOE_DEV int work_count(const Shapes& s, const Scratch& sc) {
   return n * (MODE == kGateUp ? s.I / 128 : s.d / 256);
 }
 
-template <int MODE>
+template <int MODE, bool PAIRS = false>
 MOE_DEV Work work_item(const Shapes& s, const Scratch& sc, int w) {
   Work r{};
   if (MODE == kRouter) {
@@ -163,11 +164,12 @@ MOE_DEV Work work_item(const Shapes& s, const Scratch& sc, int w) {
   }
   const int nnt = (MODE == kGateUp) ? s.I / 128 : s.d / 256;
   const int mt = w / nnt, nt = w - mt * nnt;
-  MTile m = sc.mtiles[mt];
+  MTile m = PAIRS ? sc.mpairs[mt] : sc.mtiles[mt];
+  if (!PAIRS) m.pad = 0;
   if (kDebugChecks) {
     const int total = s.T * s.k + (s.has_shared ? s.T : 0);  // grouped rows
     if (m.e < 0 || m.e > s.E || (m.e == s.E && !s.has_shared) || m.rows < 1 || m.rows > kBM || m.row0 < 0 ||
-        m.row0 + m.rows > total) {
+        m.pad < 0 || m.pad > kBM || (m.pad > 0 && m.rows != kBM) || m.row0 + m.rows + m.pad > total) {
       atomicOr(sc.status, kStatusBounds);
       m = MTile{0, 0, 1, 0};  // every role of the kernel reads the same entry and replaces it alike
     }
@@ -175,6 +177,7 @@ MOE_DEV Work work_item(const Shapes& s, const Scratch& sc, int w) {
   r.e = m.e;
   r.row0 = m.row0;
   r.rows = m.rows;
+  r.rows2 = m.pad;
   r.n0 = nt * ((MODE == kGateUp) ? 128 : 256);
   r.part = 0;
   return r;
@@ -194,7 +197,10 @@ __global__ void __launch_bounds__(Q4 ? kThreadsQ4 : kThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ GemmMaps maps, Shapes s, Scratch sc, DevCtl ctl, DevCtl drain) {
   constexpr int S = Q4 ? kStagesQ4 : (AROWS ? small_a_stages(AROWS) : kStages);  // load ring (A, and B or codes)
   constexpr int SB = Q4 ? kBStagesQ4 : S;          // B tiles the MMA reads (bf16: part of the load ring)
-  constexpr int kASlot = AROWS ? AROWS * kBK * 2 : kABytes;  // bytes per A slot
+  // 4-bit: a work item is a pair of m-tiles of one expert (both A tiles in each load stage, one
+  // expanded B tile for both); bf16: one m-tile
+  constexpr bool PAIRS = Q4 && MODE != kRouter;
+  constexpr int kASlot = PAIRS ? 2 * kABytes : (AROWS ? AROWS * kBK * 2 : kABytes);  // bytes per A slot
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* a_buf = base;
@@ -204,7 +210,7 @@ __global__ void __launch_bounds__(Q4 ? kThreadsQ4 : kThreads, 1)
   Barriers* bar = reinterpret_cast<Barriers*>(par_buf + (Q4 ? 2 * 2 * kParBytes : 0));
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int n_work = work_count<MODE>(s, sc);
+  const int n_work = work_count<MODE, PAIRS>(s, sc);
   if ((int)blockIdx.x >= n_work) return;
   const int K = (MODE == kDown) ? s.I : s.d;   // reduction length
   const int KB = K / kBK;
@@ -244,7 +250,7 @@ __global__ void __launch_bounds__(Q4 ? kThreadsQ4 : kThreads, 1)
     int it = 0, pc = 0;
     bool ok = true;
     for (int w = blockIdx.x; w < n_work && ok; w += gridDim.x) {
-      const Work wk = work_item<MODE>(s, sc, w);
+      const Work wk = work_item<MODE, PAIRS>(s, sc, w);
       const CUtensorMap* mb;
       const CUtensorMap* mp = nullptr;  // Q4: parameter view of the same rows
       int brow0, brow1 = 0;
@@ -308,19 +314,30 @@ __global__ void __launch_bounds__(Q4 ? kThreadsQ4 : kThreads, 1)
             // rows the extra box loads cost the producer more than the bytes
             // they save (the balanced T = 4096 gate/up GEMM: 229 -> 236 us
             // with boxes up to 112 rows)
-            const int a_boxes = (wk.rows + 15) / 16;
-            const bool whole = AROWS == 0 && a_boxes > 4;
-            mbar_expect_tx(&bar->full[st], (whole ? kABytes : a_boxes * 16 * kBK * 2) + tx_b);
+            const int a_boxes = (wk.rows + 15) / 16, a2_boxes = (wk.rows2 + 15) / 16;
+            const bool whole = AROWS == 0 && a_boxes > 4, whole2 = a2_boxes > 4;
+            const uint32_t a_bytes = whole ? kABytes : a_boxes * 16 * kBK * 2;
+            const uint32_t a2_bytes = PAIRS ? (whole2 ? kABytes : a2_boxes * 16 * kBK * 2) : 0u;
+            mbar_expect_tx(&bar->full[st], a_bytes + a2_bytes + tx_b);
             uint8_t* a_dst = a_buf + st * kASlot;
             uint8_t* b_dst = Q4 ? raw_buf + st * kRawBytes : b_buf + st * kBBytes;
             const int kc = kb * kBK;
+            const CUtensorMap* ma = MODE == kGateUp ? &maps.x_perm : (MODE == kDown ? &maps.h : &maps.x_tile);
+            const CUtensorMap* ma16 = MODE == kGateUp ? &maps.x_perm16 : (MODE == kDown ? &maps.h16 : &maps.x_tile16);
             if (whole) {
-              const CUtensorMap* ma = MODE == kGateUp ? &maps.x_perm : (MODE == kDown ? &maps.h : &maps.x_tile);
               tma_load_2d(a_dst, ma, kc, wk.row0, &bar->full[st], pol_a);
             } else {
-              const CUtensorMap* ma = MODE == kGateUp ? &maps.x_perm16 : (MODE == kDown ? &maps.h16 : &maps.x_tile16);
               for (int i = 0; i < a_boxes; ++i)
-                tma_load_2d(a_dst + i * 16 * kBK * 2, ma, kc, wk.row0 + 16 * i, &bar->full[st], pol_a);
+                tma_load_2d(a_dst + i * 16 * kBK * 2, ma16, kc, wk.row0 + 16 * i, &bar->full[st], pol_a);
+            }
+            if (PAIRS && wk.rows2 > 0) {  // the pair's second tile, rows row0 + 128 ...
+              if (whole2) {
+                tma_load_2d(a_dst + kABytes, ma, kc, wk.row0 + kBM, &bar->full[st], pol_a);
+              } else {
+                for (int i = 0; i < a2_boxes; ++i)
+                  tma_load_2d(a_dst + kABytes + i * 16 * kBK * 2, ma16, kc, wk.row0 + kBM + 16 * i, &bar->full[st],
+                              pol_a);
+              }
             }
             if (Q4) {  // the k block's code words: 8 per row
               if (MODE == kGateUp) {
@@ -364,14 +381,18 @@ __global__ void __launch_bounds__(Q4 ? kThreadsQ4 : kThreads, 1)
         }
       }
       for (int w = blockIdx.x; w < n_work && ok; w += gridDim.x, ++lt) {
-        const int acc = lt & 1;
-        const uint32_t use = lt >> 1;
-        if (!mbar_wait(&bar->tempty[acc], (use & 1) ^ 1, ctl) || aborted(bar)) {
+        // bf16: items alternate between the two accumulators; 4-bit pairs: every
+        // item uses both (tile 1 in columns 0..255, tile 2 in 256..511)
+        const int acc = PAIRS ? 0 : (lt & 1);
+        const uint32_t use = PAIRS ? lt : (lt >> 1);
+        if (!mbar_wait(&bar->tempty[acc], (use & 1) ^ 1, ctl) || aborted(bar) ||
+            (PAIRS && !mbar_wait(&bar->tempty[1], (use & 1) ^ 1, ctl))) {
           set_abort(bar);
           break;
         }
         tc_fence_after();
         const uint32_t d_tmem = tmem + acc * kAccCols;
+        const bool second = PAIRS && work_item<MODE, PAIRS>(s, sc, w).rows2 > 0;
         for (int kb = 0; kb < KB; ++kb, ++it) {
           const int st = it % S, sb = it % SB;
           // bf16: the stage's copies landed; 4-bit: the converters expanded the
@@ -390,11 +411,18 @@ __global__ void __launch_bounds__(Q4 ? kThreadsQ4 : kThreads, 1)
             // +32 bytes per 16-element k step inside the 128-byte swizzled row
             umma_bf16(d_tmem, ad + 2 * kk, bd + 2 * kk, idesc, (kb | kk) ? 1u : 0u);
           }
+          if (second) {
+            const uint64_t ad2 = umma_desc_sw128(smem_u32(a_buf + st * kASlot + kABytes));
+#pragma unroll
+            for (int kk = 0; kk < kBK / 16; ++kk)
+              umma_bf16(tmem + kAccCols, ad2 + 2 * kk, bd + 2 * kk, idesc, (kb | kk) ? 1u : 0u);
+          }
           umma_commit(&bar->empty[st]);
           if (Q4) umma_commit(&bar->bempty[sb]);
         }
         if (!ok) break;
         umma_commit(&bar->tfull[acc]);
+        if (PAIRS) umma_commit(&bar->tfull[1]);
       }
       umma_commit(&bar->mma_done);
       mbar_wait(&bar->mma_done, 0, drain);
@@ -405,77 +433,86 @@ __global__ void __launch_bounds__(Q4 ? kThreadsQ4 : kThreads, 1)
     const int q = warp & 3;               // TMEM lane quarter this warp may access
     const int row_local = q * 32 + lane;
     int lt = 0;
-    for (int w = blockIdx.x; w < n_work; w += gridDim.x, ++lt) {
-      const int acc = lt & 1;
-      const uint32_t use = lt >> 1;
-      if (!mbar_wait(&bar->tfull[acc], use & 1, ctl) || aborted(bar)) {
-        set_abort(bar);
-        break;
-      }
-      tc_fence_after();
-      const Work wk = work_item<MODE>(s, sc, w);
-      const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + acc * kAccCols;
-      const bool live = row_local < wk.rows;
-      if (MODE == kGateUp) {
-        uint16_t* dst = sc.h + (size_t)(wk.row0 + row_local) * s.I + wk.n0;
+    bool stop = false;
+    for (int w = blockIdx.x; w < n_work && !stop; w += gridDim.x, ++lt) {
+      const Work wk = work_item<MODE, PAIRS>(s, sc, w);
+      // bf16: one tile in the item's accumulator; 4-bit pairs: tile 1 in
+      // accumulator 0, tile 2 (rows row0 + 128 ..., maybe none) in accumulator 1
+      for (int tt = 0; tt < (PAIRS ? 2 : 1); ++tt) {
+        const int acc = PAIRS ? tt : (lt & 1);
+        const uint32_t use = PAIRS ? lt : (lt >> 1);
+        if (!mbar_wait(&bar->tfull[acc], use & 1, ctl) || aborted(bar)) {
+          set_abort(bar);
+          stop = true;
+          break;
+        }
+        tc_fence_after();
+        const int row0 = wk.row0 + tt * kBM, rows = tt ? wk.rows2 : wk.rows;
+        const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + acc * kAccCols;
+        const bool live = row_local < rows;
+        if (rows > 0) {
+          if (MODE == kGateUp) {
+            uint16_t* dst = sc.h + (size_t)(row0 + row_local) * s.I + wk.n0;
 #pragma unroll 1
-        for (int c = 0; c < 4; ++c) {
-          // the gate and up columns of the chunk: both loads, then one wait
-          uint32_t gr[32], ur[32];
-          tmem_ld32_async(taddr + c * 32, gr);
-          tmem_ld32_async(taddr + 128 + c * 32, ur);
-          tmem_ld_wait();
-          uint32_t pk[16];
+            for (int c = 0; c < 4; ++c) {
+              // the gate and up columns of the chunk: both loads, then one wait
+              uint32_t gr[32], ur[32];
+              tmem_ld32_async(taddr + c * 32, gr);
+              tmem_ld32_async(taddr + 128 + c * 32, ur);
+              tmem_ld_wait();
+              uint32_t pk[16];
 #pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const float g0 = __uint_as_float(gr[2 * j]), g1 = __uint_as_float(gr[2 * j + 1]);
-            pk[j] = pack_bf16x2(silu(g0) * __uint_as_float(ur[2 * j]), silu(g1) * __uint_as_float(ur[2 * j + 1]));
-          }
-          if (live) {
-            uint4* o = reinterpret_cast<uint4*>(dst + c * 32);
+              for (int j = 0; j < 16; ++j) {
+                const float g0 = __uint_as_float(gr[2 * j]), g1 = __uint_as_float(gr[2 * j + 1]);
+                pk[j] = pack_bf16x2(silu(g0) * __uint_as_float(ur[2 * j]), silu(g1) * __uint_as_float(ur[2 * j + 1]));
+              }
+              if (live) {
+                uint4* o = reinterpret_cast<uint4*>(dst + c * 32);
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              const uint4 v = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
-              o[j] = Q4 ? q4_chunk_order(v) : v;  // 4-bit: h is the down GEMM's A, in the expansion order
+                for (int j = 0; j < 4; ++j) {
+                  const uint4 v = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+                  o[j] = Q4 ? q4_chunk_order(v) : v;  // 4-bit: h is the down GEMM's A, in the expansion order
+                }
+              }
+            }
+          } else if (MODE == kDown) {
+            uint16_t* dst = sc.out + (size_t)(row0 + row_local) * s.d + wk.n0;
+#pragma unroll 1
+            for (int c = 0; c < 8; c += 2) {
+              // two 32-column chunks per wait
+              uint32_t v0[32], v1[32];
+              tmem_ld32_async(taddr + c * 32, v0);
+              tmem_ld32_async(taddr + (c + 1) * 32, v1);
+              tmem_ld_wait();
+              uint32_t pk[32];
+#pragma unroll
+              for (int j = 0; j < 16; ++j) {
+                pk[j] = pack_bf16x2(__uint_as_float(v0[2 * j]), __uint_as_float(v0[2 * j + 1]));
+                pk[16 + j] = pack_bf16x2(__uint_as_float(v1[2 * j]), __uint_as_float(v1[2 * j + 1]));
+              }
+              if (live) {
+                uint4* o = reinterpret_cast<uint4*>(dst + c * 32);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) o[j] = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+              }
+            }
+          } else {
+            float* dst = sc.logits + (size_t)wk.part * s.T * s.E + (size_t)(row0 + row_local) * s.E;
+#pragma unroll 1
+            for (int c = 0; c < 8; ++c) {
+              float v[32];
+              tmem_ld32(taddr + c * 32, v);
+              if (live) {
+                float4* o = reinterpret_cast<float4*>(dst + c * 32);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) o[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+              }
             }
           }
         }
-      } else if (MODE == kDown) {
-        uint16_t* dst = sc.out + (size_t)(wk.row0 + row_local) * s.d + wk.n0;
-#pragma unroll 1
-        for (int c = 0; c < 8; c += 2) {
-          // two 32-column chunks per wait
-          uint32_t v0[32], v1[32];
-          tmem_ld32_async(taddr + c * 32, v0);
-          tmem_ld32_async(taddr + (c + 1) * 32, v1);
-          tmem_ld_wait();
-          uint32_t pk[32];
-#pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            pk[j] = pack_bf16x2(__uint_as_float(v0[2 * j]), __uint_as_float(v0[2 * j + 1]));
-            pk[16 + j] = pack_bf16x2(__uint_as_float(v1[2 * j]), __uint_as_float(v1[2 * j + 1]));
-          }
-          if (live) {
-            uint4* o = reinterpret_cast<uint4*>(dst + c * 32);
-#pragma unroll
-            for (int j = 0; j < 8; ++j) o[j] = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
-          }
-        }
-      } else {
-        float* dst = sc.logits + (size_t)wk.part * s.T * s.E + (size_t)(wk.row0 + row_local) * s.E;
-#pragma unroll 1
-        for (int c = 0; c < 8; ++c) {
-          float v[32];
-          tmem_ld32(taddr + c * 32, v);
-          if (live) {
-            float4* o = reinterpret_cast<float4*>(dst + c * 32);
-#pragma unroll
-            for (int j = 0; j < 8; ++j) o[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
-          }
-        }
+        tc_fence_before();
+        mbar_arrive(&bar->tempty[acc]);
       }
-      tc_fence_before();
-      mbar_arrive(&bar->tempty[acc]);
     }
   } else if (Q4) {
     // ------------------------------------------------------------ code expansion (4-bit)

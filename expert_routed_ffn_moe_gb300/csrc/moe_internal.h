@@ -34,7 +34,8 @@ struct Scratch {
   int* perm;              // [T*k + T]: token of each grouped row; rows T*k.. are the shared expert's
   int* slot;              // [T, k]: grouped row of (t, idx[t][j])
   MTile* mtiles;          // grouped-GEMM m-tiles
-  int* meta;              // [0] = number of m-tiles, [1] = number of active experts
+  MTile* mpairs;          // the m-tiles two by two within each expert group (pad = rows of the second, 0: none)
+  int* meta;              // [0] = number of m-tiles, [1] = number of active experts, [2] = number of m-tile pairs
   int* active;            // [E + 1]: experts with count > 0, ascending, then the shared expert
   unsigned* tickets;      // last-block counters (self-resetting)
   uint16_t* x_perm;       // [T*k + T, d] bf16 token rows in grouped order (GEMM path)

@@ -347,11 +347,34 @@ __global__ void __launch_bounds__(256) group_scan_kernel(Shapes s, Scratch sc) {
     m.pad = 0;
     sc.mtiles[mt_total + i] = m;
   }
+  // the same tiles two by two within each group (the 4-bit GEMMs expand each
+  // weight tile once for both tiles of a pair)
+  const int np = (nm + 1) / 2;
+  int np_total;
+  const int np_off = block_exclusive_scan(np, &np_total);
+  for (int i = 0; i < np; ++i) {
+    MTile m;
+    m.e = tid;
+    m.row0 = off + 2 * i * kBM;
+    m.rows = min(kBM, cnt - 2 * i * kBM);
+    m.pad = max(0, min(kBM, cnt - (2 * i + 1) * kBM));
+    sc.mpairs[np_off + i] = m;
+  }
+  const int snp = (snm + 1) / 2;
+  for (int i = tid; i < snp; i += blockDim.x) {
+    MTile m;
+    m.e = s.E;
+    m.row0 = total + 2 * i * kBM;
+    m.rows = min(kBM, shared_cnt - 2 * i * kBM);
+    m.pad = max(0, min(kBM, shared_cnt - (2 * i + 1) * kBM));
+    sc.mpairs[np_total + i] = m;
+  }
   int n_act;
   const int apos = block_exclusive_scan(cnt > 0 ? 1 : 0, &n_act);
   if (cnt > 0) sc.active[apos] = tid;
   if (tid == 0) {
     if (s.has_shared) sc.active[n_act] = s.E;
+    sc.meta[2] = np_total + snp;
     sc.meta[0] = mt_total + snm;
     sc.meta[1] = n_act + (s.has_shared ? 1 : 0);
     sc.tickets[0] = 0u;  // ready for the next launch
