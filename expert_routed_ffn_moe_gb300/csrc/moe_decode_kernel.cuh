@@ -102,6 +102,22 @@ MOE_DEV float value_of(unsigned long long w) { return __uint_as_float((unsigned)
 // against one float4 of activations.  A lane takes chunk lane + 32 c, so a
 // warp reads 256 contiguous weight bytes and 512 contiguous activation bytes
 // per step: no shared-memory bank conflicts on either side.
+// Packed fp32 pairs (fma.rn.f32x2: two independent FMAs in one instruction).
+MOE_DEV unsigned long long pk2(float lo, float hi) {
+  unsigned long long r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+MOE_DEV unsigned long long ffma2(unsigned long long a, unsigned long long b, unsigned long long c) {
+  unsigned long long d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+MOE_DEV float sum2(unsigned long long v) {
+  float lo, hi;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+  return lo + hi;
+}
 MOE_DEV void dot4x2(const uint2 g, const uint2 u, const float4 a, float& gs, float& us) {
   gs = fmaf(bf16_lo(g.x), a.x, gs);
   us = fmaf(bf16_lo(u.x), a.x, us);
@@ -301,14 +317,13 @@ MOE_DEV float q4_one_plus(uint32_t w) {
 // sum_i (1 + q_i / 16) a_i over the 8 codes of word w and a[0..7] (two
 // independent chains, so consecutive FMAs do not wait on each other)
 MOE_DEV float q4_dot8(uint32_t w, const float4 a0, const float4 a1) {
-  float r = q4_one_plus<0>(w) * a0.x, t = q4_one_plus<4>(w) * a1.x;
-  r = fmaf(q4_one_plus<1>(w), a0.y, r);
-  t = fmaf(q4_one_plus<5>(w), a1.y, t);
-  r = fmaf(q4_one_plus<2>(w), a0.z, r);
-  t = fmaf(q4_one_plus<6>(w), a1.z, t);
-  r = fmaf(q4_one_plus<3>(w), a0.w, r);
-  t = fmaf(q4_one_plus<7>(w), a1.w, t);
-  return r + t;
+  // codes 0..7 against a0.xyzw, a1.xyzw as (even, odd) pairs: two chains of
+  // two packed FMAs
+  unsigned long long r = ffma2(pk2(q4_one_plus<0>(w), q4_one_plus<1>(w)), pk2(a0.x, a0.y), 0ull);
+  unsigned long long t = ffma2(pk2(q4_one_plus<4>(w), q4_one_plus<5>(w)), pk2(a1.x, a1.y), 0ull);
+  r = ffma2(pk2(q4_one_plus<2>(w), q4_one_plus<3>(w)), pk2(a0.z, a0.w), r);
+  t = ffma2(pk2(q4_one_plus<6>(w), q4_one_plus<7>(w)), pk2(a1.z, a1.w), t);
+  return sum2(r) + sum2(t);
 }
 // One word's share of a 4-bit row dot product: with sum_i (1 + q_i/16) a_i =
 // raw and sum_i a_i = as, sum_i (s q_i + b) a_i = 16 s raw + (b - 16 s) as.
