@@ -385,8 +385,7 @@ __global__ void __launch_bounds__(Q4 ? kThreadsQ4 : kThreads, 1)
         // item uses both (tile 1 in columns 0..255, tile 2 in 256..511)
         const int acc = PAIRS ? 0 : (lt & 1);
         const uint32_t use = PAIRS ? lt : (lt >> 1);
-        if (!mbar_wait(&bar->tempty[acc], (use & 1) ^ 1, ctl) || aborted(bar) ||
-            (PAIRS && !mbar_wait(&bar->tempty[1], (use & 1) ^ 1, ctl))) {
+        if (!mbar_wait(&bar->tempty[acc], (use & 1) ^ 1, ctl) || aborted(bar)) {
           set_abort(bar);
           break;
         }
@@ -411,7 +410,15 @@ __global__ void __launch_bounds__(Q4 ? kThreadsQ4 : kThreads, 1)
             // +32 bytes per 16-element k step inside the 128-byte swizzled row
             umma_bf16(d_tmem, ad + 2 * kk, bd + 2 * kk, idesc, (kb | kk) ? 1u : 0u);
           }
+          if (PAIRS && kb == 0 && !mbar_wait(&bar->tempty[1], (use & 1) ^ 1, ctl)) {
+            // accumulator 1 is drained only now: the epilogue's second half
+            // overlaps this item's first k block on accumulator 0
+            set_abort(bar);
+            ok = false;
+            break;
+          }
           if (second) {
+            tc_fence_after();
             const uint64_t ad2 = umma_desc_sw128(smem_u32(a_buf + st * kASlot + kABytes));
 #pragma unroll
             for (int kk = 0; kk < kBK / 16; ++kk)
