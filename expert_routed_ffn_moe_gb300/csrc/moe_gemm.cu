@@ -35,12 +35,15 @@
 // loads each k block's raw codes (256 rows x 32 bytes) and, every 8 k blocks,
 // the rows' scales and biases of those 8 groups; 8 more warps expand the codes
 // to bf16, w = s q + b rounded once (bf16x2 fma), straight into the 128-byte
-// swizzled B tile the MMA reads, then release it to the MMA issuer.  The loads
-// run in a 5-stage ring of (A 16 KB + codes 8 KB) and the expanded B tiles in
-// a 2-stage ring of 32 KB, so that the copies in flight cover the memory
-// latency while expansion and MMA overlap (one 3-stage ring of A + codes + B
-// kept only 3 loads in flight and ran the gate/up GEMM 2.3 times slower than
-// its tensor time); plus two 8 KB parameter buffers.
+// swizzled B tile the MMA reads, then release it to the MMA issuer.  A work
+// item is a pair of m-tiles of one expert, so each expanded tile serves two
+// tiles' MMAs.  The loads run in a 3-stage ring of (two A tiles 32 KB + codes
+// 8 KB) and the expanded B tiles in a 2-stage ring of 32 KB, so that the
+// copies in flight cover the memory latency while expansion and MMA overlap;
+// plus two 8 KB parameter buffers.
+//
+// bf16 gate/up at large batches (T k >= 512 E) also runs pairs: a 3-stage ring
+// of (two A tiles + one B tile), see grouped_gemm_kernel.
 #include "moe_internal.h"
 
 namespace moe {
@@ -83,6 +86,10 @@ struct __align__(8) Barriers {
 };
 
 constexpr size_t kSmemBytes = 1024 /*align slack*/ + (size_t)kStages * (kABytes + kBBytes) + sizeof(Barriers);
+// bf16 pairs (gate/up at large batches): a load stage holds both A tiles of a
+// pair and one B tile, 64 KB instead of 48 KB for twice the MMA work
+constexpr int kStagesPairs = 3;
+constexpr size_t kSmemBytesPairs = 1024 + (size_t)kStagesPairs * (2 * kABytes + kBBytes) + sizeof(Barriers);
 // Small batches (every expert group, the shared one included, has at most
 // AROWS <= T rows): an A slot holds only AROWS rows (2 or 4 KB), which frees
 // shared memory for more weight stages in flight.  The MMA still reads 128 rows
@@ -96,7 +103,8 @@ constexpr size_t small_a_smem(int arows) {
 }
 constexpr size_t kSmemBytesQ4 = 1024 + (size_t)kStagesQ4 * (2 * kABytes + kRawBytes) + (size_t)kBStagesQ4 * kBBytes +
                                 2 * 2 * kParBytes + sizeof(Barriers);
-static_assert(kSmemBytesQ4 <= 227 * 1024 && kSmemBytes <= 227 * 1024, "shared memory of one CTA");
+static_assert(kSmemBytesQ4 <= 227 * 1024 && kSmemBytes <= 227 * 1024 && kSmemBytesPairs <= 227 * 1024,
+              "shared memory of one CTA");
 static_assert(small_a_stages(16) <= kMaxStages && small_a_stages(32) <= kMaxStages && kStagesQ4 <= kMaxStages,
               "barrier arrays");
 static_assert(small_a_smem(16) <= 227 * 1024 && small_a_smem(32) <= 227 * 1024, "shared memory of one CTA");
@@ -134,7 +142,7 @@ MOE_DEV void tma_load_2d_nohint(void* dst, const CUtensorMap* m, int c0, int c1,
 
 struct Work {
   int e, row0, rows;   // expert (E = shared), first grouped row, valid rows
-  int rows2;           // 4-bit: valid rows of the pair's second tile (rows row0 + 128 ...; 0: none)
+  int rows2;           // pairs: valid rows of the pair's second tile (rows row0 + 128 ...; 0: none)
   int n0;              // first output column of the tile (B row offset inside the expert)
   int part;            // router: 0 / 1 / 2 = hi / mid / lo weight term
 };
@@ -192,14 +200,18 @@ MOE_DEV void set_abort(Barriers* b) { *reinterpret_cast<volatile int*>(&b->abort
 // warps 6 .. 6 + kConvWarps - 1 (gate/up and down modes only).
 // AROWS (bf16 only): 0 = full 128-row A slots; 16 or 32 = the small-batch
 // layout above (valid only when T <= AROWS).
-template <int MODE, bool Q4, int AROWS = 0>
+// PAIRED: a work item is a pair of m-tiles of one expert, both multiplied by
+// each B tile the item loads (always for 4-bit; for bf16 an option of the
+// full-slot layout).  Each SM then takes in 64 KB per k block for two tiles'
+// MMAs instead of 2 x 48 KB, which pays where groups are long (pairs_for).
+template <int MODE, bool Q4, int AROWS = 0, bool PAIRED = Q4>
 __global__ void __launch_bounds__(Q4 ? kThreadsQ4 : kThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ GemmMaps maps, Shapes s, Scratch sc, DevCtl ctl, DevCtl drain) {
-  constexpr int S = Q4 ? kStagesQ4 : (AROWS ? small_a_stages(AROWS) : kStages);  // load ring (A, and B or codes)
+  static_assert(!(PAIRED && AROWS), "pairs use full A slots");
+  constexpr bool PAIRS = PAIRED && MODE != kRouter;
+  // load ring (A, and B or codes)
+  constexpr int S = Q4 ? kStagesQ4 : (AROWS ? small_a_stages(AROWS) : (PAIRS ? kStagesPairs : kStages));
   constexpr int SB = Q4 ? kBStagesQ4 : S;          // B tiles the MMA reads (bf16: part of the load ring)
-  // 4-bit: a work item is a pair of m-tiles of one expert (both A tiles in each load stage, one
-  // expanded B tile for both); bf16: one m-tile
-  constexpr bool PAIRS = Q4 && MODE != kRouter;
   constexpr int kASlot = PAIRS ? 2 * kABytes : (AROWS ? AROWS * kBK * 2 : kABytes);  // bytes per A slot
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -381,8 +393,8 @@ __global__ void __launch_bounds__(Q4 ? kThreadsQ4 : kThreads, 1)
         }
       }
       for (int w = blockIdx.x; w < n_work && ok; w += gridDim.x, ++lt) {
-        // bf16: items alternate between the two accumulators; 4-bit pairs: every
-        // item uses both (tile 1 in columns 0..255, tile 2 in 256..511)
+        // single tiles alternate between the two accumulators; pairs use both
+        // (tile 1 in columns 0..255, tile 2 in 256..511)
         const int acc = PAIRS ? 0 : (lt & 1);
         const uint32_t use = PAIRS ? lt : (lt >> 1);
         if (!mbar_wait(&bar->tempty[acc], (use & 1) ^ 1, ctl) || aborted(bar)) {
@@ -443,8 +455,8 @@ __global__ void __launch_bounds__(Q4 ? kThreadsQ4 : kThreads, 1)
     bool stop = false;
     for (int w = blockIdx.x; w < n_work && !stop; w += gridDim.x, ++lt) {
       const Work wk = work_item<MODE, PAIRS>(s, sc, w);
-      // bf16: one tile in the item's accumulator; 4-bit pairs: tile 1 in
-      // accumulator 0, tile 2 (rows row0 + 128 ..., maybe none) in accumulator 1
+      // single tiles: the item's accumulator; pairs: tile 1 in accumulator 0,
+      // tile 2 (rows row0 + 128 ..., maybe none) in accumulator 1
       for (int tt = 0; tt < (PAIRS ? 2 : 1); ++tt) {
         const int acc = PAIRS ? tt : (lt & 1);
         const uint32_t use = PAIRS ? lt : (lt >> 1);
@@ -572,6 +584,16 @@ __global__ void __launch_bounds__(Q4 ? kThreadsQ4 : kThreads, 1)
   if (warp == 1) tmem_dealloc(tmem, kTmemCols);
 }
 
+// bf16 pairs for the gate/up GEMM once the mean group (T k / E rows) spans 4
+// tiles.  Measured per launch at d = 2048, 256 experts of 512, top-8 + shared:
+// T = 32768 (8 tiles a group) 868 -> 782 us with pairs; T = 4096 (1 tile a
+// group) balanced 219 -> 238 us and skewed (3.5 tiles per active expert)
+// 166 -> 170 us, where the second tiles are short or missing and the 3-stage
+// ring keeps fewer copies in flight than the 4-stage one.
+static bool pairs_for(int mode, const Shapes& s) {
+  return mode == kGateUp && (long long)s.T * s.k >= 4LL * s.E * kBM;
+}
+
 template <int MODE>
 static cudaError_t launch_mode(const Shapes& s, const GemmMaps& m, const Scratch& sc, const DevCtl& ctl,
                                int num_sms, cudaStream_t st) {
@@ -584,6 +606,8 @@ static cudaError_t launch_mode(const Shapes& s, const GemmMaps& m, const Scratch
     grouped_gemm_kernel<MODE, false, 16><<<num_sms, kThreads, small_a_smem(16), st>>>(m, s, sc, ctl, drain);
   else if (MODE != kRouter && s.T <= 32)
     grouped_gemm_kernel<MODE, false, 32><<<num_sms, kThreads, small_a_smem(32), st>>>(m, s, sc, ctl, drain);
+  else if (pairs_for(MODE, s))
+    grouped_gemm_kernel<kGateUp, false, 0, true><<<num_sms, kThreads, kSmemBytesPairs, st>>>(m, s, sc, ctl, drain);
   else
     grouped_gemm_kernel<MODE, false><<<num_sms, kThreads, kSmemBytes, st>>>(m, s, sc, ctl, drain);
   return cudaGetLastError();
@@ -594,6 +618,11 @@ cudaError_t prepare_gemm_kernels() {
                       (const void*)grouped_gemm_kernel<kRouter, false>};
   for (const void* k : ks) {
     cudaError_t err = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+    if (err != cudaSuccess) return err;
+  }
+  {
+    cudaError_t err = cudaFuncSetAttribute((const void*)grouped_gemm_kernel<kGateUp, false, 0, true>,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytesPairs);
     if (err != cudaSuccess) return err;
   }
   const void* kq[] = {(const void*)grouped_gemm_kernel<kGateUp, true>, (const void*)grouped_gemm_kernel<kDown, true>};

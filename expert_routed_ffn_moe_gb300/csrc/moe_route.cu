@@ -347,8 +347,19 @@ __global__ void __launch_bounds__(256) group_scan_kernel(Shapes s, Scratch sc) {
     m.pad = 0;
     sc.mtiles[mt_total + i] = m;
   }
-  // the same tiles two by two within each group (the 4-bit GEMMs expand each
-  // weight tile once for both tiles of a pair)
+  // the same tiles two by two within each group (the paired GEMMs load or
+  // expand each weight tile once for both tiles of a pair).  The shared
+  // expert's pairs, all full but the last, come first: the persistent GEMMs
+  // take items in list order, so the heaviest are not left for the end.
+  const int snp = (snm + 1) / 2;
+  for (int i = tid; i < snp; i += blockDim.x) {
+    MTile m;
+    m.e = s.E;
+    m.row0 = total + 2 * i * kBM;
+    m.rows = min(kBM, shared_cnt - 2 * i * kBM);
+    m.pad = max(0, min(kBM, shared_cnt - (2 * i + 1) * kBM));
+    sc.mpairs[i] = m;
+  }
   const int np = (nm + 1) / 2;
   int np_total;
   const int np_off = block_exclusive_scan(np, &np_total);
@@ -358,16 +369,7 @@ __global__ void __launch_bounds__(256) group_scan_kernel(Shapes s, Scratch sc) {
     m.row0 = off + 2 * i * kBM;
     m.rows = min(kBM, cnt - 2 * i * kBM);
     m.pad = max(0, min(kBM, cnt - (2 * i + 1) * kBM));
-    sc.mpairs[np_off + i] = m;
-  }
-  const int snp = (snm + 1) / 2;
-  for (int i = tid; i < snp; i += blockDim.x) {
-    MTile m;
-    m.e = s.E;
-    m.row0 = total + 2 * i * kBM;
-    m.rows = min(kBM, shared_cnt - 2 * i * kBM);
-    m.pad = max(0, min(kBM, shared_cnt - (2 * i + 1) * kBM));
-    sc.mpairs[np_total + i] = m;
+    sc.mpairs[snp + np_off + i] = m;
   }
   int n_act;
   const int apos = block_exclusive_scan(cnt > 0 ? 1 : 0, &n_act);

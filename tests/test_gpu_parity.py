@@ -93,6 +93,20 @@ def test_gemv_and_gemm_paths_agree_fp32_x():
     assert a[0] < 1e-2 and b[0] < 1e-2
 
 
+@pytest.mark.parametrize("w", [
+    # groups of ~512 rows: two full pairs, some a single tile more; the shared group 8 tiles
+    custom("pairs_e8", T=1024, E=8, k=4),
+    # groups of ~525 rows: two full pairs and a single tile; the shared group's last pair is part-filled
+    custom("pairs_e4", T=700, E=4, k=3),
+    # ragged groups of ~525 rows, no shared expert
+    custom("pairs_e16_noshared", T=2100, E=16, k=4, I_s=0),
+], ids=lambda w: w.name)
+def test_paired_gate_up_groups(w):
+    # T k >= 512 E: the gate/up GEMM multiplies two m-tiles of a group per weight tile
+    assert w.T * w.k >= 4 * 128 * w.E
+    full_case(w)
+
+
 @pytest.mark.parametrize("path", [moe.MOE_PATH_GEMV, moe.MOE_PATH_GEMM])
 def test_no_shared_expert(path):
     full_case(custom("noshared", T=8, I_s=0), path=path)
