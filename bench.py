@@ -26,7 +26,11 @@ path is bracketed by its own CUDA events inside the replayed graph (through the
 library's profiling hook), which gives its average launch duration for the
 roofline.  ``e2e`` repeats the measurement with each step's x (every layer's
 tokens, one pinned block) copied in from host memory and y copied back out, one
-copy each way per step, inside the timed region.
+copy each way per step, inside the timed region.  As a serving loop would, it
+overlaps the copies with the layers of the neighbouring steps: device x and y
+are double-buffered, step s + 1's upload and step s - 1's download run on two
+copy streams while step s computes, ordered by events on the buffer each step
+reuses.
 
 Multi-GPU (torchrun): every rank runs the same workload on its own GPU (data
 parallel replicas, no collective on the data path); ``value`` counts the
@@ -410,6 +414,10 @@ def run_ours(args, rank, world, dev, workload=None, cpu_seconds=None, chunk=None
     yd_all = torch.empty_like(xd_all)
     yh_all = torch.empty_like(xh_all).pin_memory()
     xh, xd, yd, yh = list(xh_all), list(xd_all), list(yd_all), list(yh_all)
+    # end-to-end steps: two device buffers for x and for y, and the copy streams
+    xd2, yd2 = [xd_all, torch.empty_like(xd_all)], [yd_all, torch.empty_like(yd_all)]
+    cs_in, cs_out = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+    ev_in, ev_done, ev_out = ([torch.cuda.Event() for _ in range(2)] for _ in range(3))
     max_tokens = chunk if chunk else w.T
     ctx = moe.MoeLayer(w.d, w.E, w.I, w.k, max_tokens, x_dtype=moe.MOE_F32 if w.x_dtype == "f32" else moe.MOE_BF16,
                        has_router_bias=w.skewed, has_shared=w.I_s > 0, shared_gate=args.shared_gate,
@@ -432,13 +440,27 @@ def run_ours(args, rank, world, dev, workload=None, cpu_seconds=None, chunk=None
         # weights while the previous layer's kernel finishes (moe_set_overlap)
         moe.moe_set_overlap(ctx.ctx, True)
 
-    def step(ev_pair=None, e2e=False):
+    def step(ev_pair=None, e2e=False, s=0):
         if ev_pair is not None and whole_layer:
             # every launch of the step is the dominant kernel: bracket the
             # step's back-to-back launches with one event pair
             moe.moe_record_event(ev_pair[0], stream)
+        xs, ys = xd, yd
         if e2e:
-            xd_all.copy_(xh_all, non_blocking=True)
+            # upload into buffer b once step s - 2's layers are done reading it
+            # (step 0 joins the copy stream behind the stream's earlier work)
+            b = s & 1
+            if s == 0:
+                cs_in.wait_stream(stream)
+            elif s >= 2:
+                cs_in.wait_event(ev_done[b])
+            with torch.cuda.stream(cs_in):
+                xd2[b].copy_(xh_all, non_blocking=True)
+            ev_in[b].record(cs_in)
+            stream.wait_event(ev_in[b])
+            if s >= 2:
+                stream.wait_event(ev_out[b])  # step s - 2's download of y buffer b is done
+            xs, ys = list(xd2[b]), list(yd2[b])
         for L in range(layers):
             if ev_pair is not None and L == 0 and not whole_layer:
                 moe.moe_time_kernel(ctx.ctx, dom, *ev_pair)
@@ -446,10 +468,14 @@ def run_ours(args, rank, world, dev, workload=None, cpu_seconds=None, chunk=None
             if layers > 1:  # stacked layers: name the next layer's first reads as a prefetch hint
                 q = weights[(L + 1) % layers]
                 moe.moe_set_prefetch(ctx.ctx, q["router_w"], q["shared"])
-            moe.moe_forward(ctx.ctx, xd[L], p["router_w"], p["router_b"], p["gate_up"], p["down"], p["shared"], w.k,
-                            yd[L], stream, packed_weights=q4)
+            moe.moe_forward(ctx.ctx, xs[L], p["router_w"], p["router_b"], p["gate_up"], p["down"], p["shared"], w.k,
+                            ys[L], stream, packed_weights=q4)
         if e2e:
-            yh_all.copy_(yd_all, non_blocking=True)
+            ev_done[b].record(stream)
+            cs_out.wait_event(ev_done[b])
+            with torch.cuda.stream(cs_out):
+                yh_all.copy_(yd2[b], non_blocking=True)
+            ev_out[b].record(cs_out)
         if ev_pair is not None and whole_layer:
             moe.moe_record_event(ev_pair[1], stream)
 
@@ -489,7 +515,10 @@ def run_ours(args, rank, world, dev, workload=None, cpu_seconds=None, chunk=None
         before = moe.moe_launch_count(ctx.ctx)
         with torch.cuda.graph(g, stream=stream):
             for s in range(n_steps):
-                step(evs[sampled.index(s)] if s in sampled else None, e2e)
+                step(evs[sampled.index(s)] if s in sampled else None, e2e, s)
+            if e2e:  # join the copy streams: the graph ends when the last download has landed
+                stream.wait_stream(cs_in)
+                stream.wait_stream(cs_out)
         launches = moe.moe_launch_count(ctx.ctx) - before
         return g, evs, launches
 
@@ -529,6 +558,10 @@ def run_ours(args, rank, world, dev, workload=None, cpu_seconds=None, chunk=None
     ms, kern_ms, launches = timed(args.steps, e2e=False)
     clk = clocks.stop()
     ms_e2e, _, _ = timed(args.steps, e2e=True)
+    # the downloaded y of the last end-to-end step must be the device run's y, bit for bit
+    torch.cuda.synchronize(dev)
+    if not all(torch.equal(yh_all, yd2[b].cpu()) for b in range(min(2, args.steps))):
+        raise RuntimeError("end-to-end steps returned a y that differs from the device-resident run")
     st = ctx.status()
     if st != moe.MOE_OK:
         raise RuntimeError("device status after timing: " + moe.moe_strerror(st))
@@ -608,7 +641,9 @@ def run_ours(args, rank, world, dev, workload=None, cpu_seconds=None, chunk=None
                                **({"shared_gate": "sigmoid"} if args.shared_gate else {})),
                    e2e=dict(value=round(e2e_value, 1), unit=UNIT,
                             h2d_bytes_per_step=int(sum(t.numel() * t.element_size() for t in xh)),
-                            d2h_bytes_per_step=int(sum(t.numel() * t.element_size() for t in yh))),
+                            d2h_bytes_per_step=int(sum(t.numel() * t.element_size() for t in yh)),
+                            copies="overlapped with the neighbouring steps' layers: two copy streams, "
+                                   "double-buffered device x and y"),
                    gpu_launches=int(launches), roofline=roof, layer=whole, clocks=clk, cpu_baseline=cpu)
     ctx.close()
     return out
