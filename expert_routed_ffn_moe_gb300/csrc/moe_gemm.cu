@@ -256,13 +256,25 @@ __global__ void __launch_bounds__(Q4 ? kThreadsQ4 : kThreads, 1)
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) tma_prefetch_desc(MODE == kGateUp ? &maps.x_perm : (MODE == kDown ? &maps.h : &maps.x_tile));
-    const uint64_t pol_w = policy_evict_normal();  // several m-tiles of one expert reuse its weights
+    const uint64_t pol_reuse = policy_evict_normal();  // several m-tiles of one expert reuse its weights
+    const uint64_t pol_once = policy_evict_first();    // ... or are read by one item only
     const uint64_t pol_a = policy_evict_last();
     constexpr uint32_t tx_b = Q4 ? kRawBytes : kBBytes;
     int it = 0, pc = 0;
     bool ok = true;
     for (int w = blockIdx.x; w < n_work && ok; w += gridDim.x) {
       const Work wk = work_item<MODE, PAIRS>(s, sc, w);
+      // bf16 weight tiles of a group that fits one item (one m-tile, or a
+      // pair) are read once: stream them, so that they do not push the token
+      // rows, which every n-tile of the group reads, out of L2 (T = 32 layer
+      // 197 -> 190 us, T = 128 292 -> 285 us, skewed T = 4096 371 -> 366 us).
+      // A group of more tiles reads them again from later items (balanced
+      // T = 4096, where half the groups spill a few rows into a second tile:
+      // 435 -> 464 us per layer when those were streamed too), and a 4-bit
+      // k block reads 32 bytes of each code row, so four k blocks share a line
+      // (gate/up 253 -> 259 us when streamed)
+      const int group_rows = MODE == kRouter ? 0 : (wk.e < s.E ? sc.counts[wk.e] : s.T);
+      const uint64_t pol_w = (!Q4 && MODE != kRouter && group_rows <= (PAIRS ? 2 : 1) * kBM) ? pol_once : pol_reuse;
       const CUtensorMap* mb;
       const CUtensorMap* mp = nullptr;  // Q4: parameter view of the same rows
       int brow0, brow1 = 0;
