@@ -600,8 +600,10 @@ __global__ void __launch_bounds__(Q4 ? kThreadsQ4 : kThreads, 1)
 // tiles.  Measured per launch at d = 2048, 256 experts of 512, top-8 + shared:
 // T = 32768 (8 tiles a group) 868 -> 782 us with pairs; T = 4096 (1 tile a
 // group) balanced 219 -> 238 us and skewed (3.5 tiles per active expert)
-// 166 -> 170 us, where the second tiles are short or missing and the 3-stage
-// ring keeps fewer copies in flight than the 4-stage one.
+// 166 -> 170 us.  There the mean CTA finishes its loop sooner with pairs
+// (skewed: 136 vs 144 us), but the items are twice as long, so the slowest
+// CTA ends later than with single tiles, and a pair's two accumulators both
+// wait for the epilogue before the next item starts.
 static bool pairs_for(int mode, const Shapes& s) {
   return mode == kGateUp && (long long)s.T * s.k >= 4LL * s.E * kBM;
 }
