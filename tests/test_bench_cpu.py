@@ -80,3 +80,30 @@ def test_q4_bytes_and_plane_roundtrip():
     words, scales, biases = bench.unpack_q4_planes(buf, w.E, w.d, w.I)
     assert np.array_equal(words, q["dn_words"]) and np.array_equal(scales, q["dn_scales"])
     assert np.array_equal(biases, q["dn_biases"])
+
+
+def test_committed_traffic_records_are_well_formed():
+    # every ncu summary's record names a kernel whose sources bench.py hashes
+    # and a workload it runs (variant suffixes included), and gives a byte
+    # count; a record of stale sources is allowed (it just stops matching)
+    import glob
+    import re
+
+    import moe_workloads as mw
+
+    pat = re.compile(r"traffic-record: kernel=(\S+) workload=(\S+) source_sha256=([0-9a-f]{16}) bytes_per_launch=(\d+)$")
+    n = 0
+    for path in sorted(glob.glob(os.path.join(bench.HERE, "profiles", "*.md"))):
+        for line in open(path):
+            if not line.startswith("traffic-record:"):
+                continue
+            m = pat.match(line.strip())
+            assert m, (path, line)
+            kernel, workload, _, nbytes = m.groups()
+            assert kernel in bench.KERNEL_SOURCES, (path, kernel)
+            base = workload.split("+")[0]
+            assert base in mw.WORKLOADS, (path, workload)
+            assert all(v in ("q4", "shared_gate") or v.startswith("chunk") for v in workload.split("+")[1:]), workload
+            assert int(nbytes) > 0
+            n += 1
+    assert n > 0
